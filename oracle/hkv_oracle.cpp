@@ -1,0 +1,420 @@
+// hkv_oracle.cpp -- reference model of the cache-semantic hash table.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the correctness oracle that the
+// CUDA library is checked against.  Only the test suite, the smoke check in
+// __graft_entry__.py and the cpu_baseline leg of bench.py may load it.  The
+// product path (hash_table_cache_gb300/) never links, imports or calls it,
+// and this file shares no header, helper or constant with that path.
+//
+// It is deliberately plain: single-threaded, one std::vector per bucket,
+// linear scans, no blocking or reordering beyond what the method states.
+//
+// Source of the method: "HierarchicalKV: A GPU Hash Table with Cache
+// Semantics for Continuous Online Embedding Storage" (arXiv 2603.17168v1),
+// cited below as HKV with its section / algorithm / proposition numbers.
+//
+// Readings taken where the paper is silent or inconsistent (each one is also
+// listed in the design notes of the repository):
+//  R1 hash: the paper says only "derived from Murmur3"; we use the 64-bit
+//     MurmurHash3 finalizer (Appleby, public domain) as H(k).
+//  R2 bucket b1 = H(k) mod B.  Dual mode: b2 = H(k ^ 0x9E3779B97F4A7C15) mod B,
+//     and b2 = (b1 + 1) mod B when the two coincide.
+//  R3 the 16 keys 0xFFFFFFFFFFFFFFF0..0xFFFFFFFFFFFFFFFF are reserved
+//     sentinels (EMPTY and LOCKED live there); inputs carrying them are
+//     skipped and counted.
+//  R4 rank of an entry = (score, key), compared lexicographically as
+//     unsigned integers.  Admission and victim choice use the rank, which
+//     breaks the paper's equal-score ties deterministically.
+//  R5 duplicate keys inside one batch collapse to their last occurrence.
+//  R6 within one batch, the unique keys are applied in this serial order:
+//     first every key that is already resident (in-place update, HKV
+//     Algorithm 2's found branch), then every absent key (the empty-slot /
+//     eviction / rejection branches), each group in batch order.  The paper
+//     runs a batch in parallel and fixes no order; this is one valid serial
+//     order, and when no update lowers a rank it gives the same table as any
+//     other serial order.
+//  R7 scores == NULL: every key of the call gets the table's step counter,
+//     which starts at 1 and increments once per insert_or_assign call (the
+//     STEP strategy of the DynamicEmb API page).
+//  R8 find of an absent key leaves the caller's value and score outputs
+//     untouched and reports found = 0.
+//  R9 slot positions are not modelled: a bucket is an unordered set of at
+//     most 128 entries; nothing observable depends on positions.
+//  The 8-bit digest only accelerates lookups and never changes a result
+//  (HKV §3.2), so the oracle does not model it.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+namespace {
+
+constexpr int kSlots = 128;                                 // HKV §3.2: S = 128
+constexpr uint64_t kReservedLo = 0xFFFFFFFFFFFFFFF0ull;    // R3
+constexpr uint64_t kDualSeed = 0x9E3779B97F4A7C15ull;      // R2
+
+// MurmurHash3 64-bit finalizer (R1).
+uint64_t murmur_fmix64(uint64_t h) {
+    h ^= h >> 33;
+    h *= 0xff51afd7ed558ccdull;
+    h ^= h >> 33;
+    h *= 0xc4ceb9fe1a85ec53ull;
+    h ^= h >> 33;
+    return h;
+}
+
+bool is_reserved(uint64_t k) { return k >= kReservedLo; }
+
+// R4: rank comparison.
+bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
+    return s1 < s2 || (s1 == s2 && k1 < k2);
+}
+
+struct Bucket {
+    // Parallel arrays, unordered, size <= kSlots (R9).
+    std::vector<uint64_t> keys;
+    std::vector<uint64_t> scores;
+    std::vector<float> values;   // keys.size() * dim
+
+    int find(uint64_t k) const {
+        for (size_t i = 0; i < keys.size(); ++i)
+            if (keys[i] == k) return static_cast<int>(i);
+        return -1;
+    }
+    int size() const { return static_cast<int>(keys.size()); }
+    // Position of the minimum-rank entry (HKV Algorithm 2, arg-min over the
+    // bucket's scores, ties by key per R4).  Bucket must be non-empty.
+    int argmin_rank() const {
+        int m = 0;
+        for (int i = 1; i < size(); ++i)
+            if (rank_less(scores[i], keys[i], scores[m], keys[m])) m = i;
+        return m;
+    }
+};
+
+struct Counts {
+    uint64_t updated = 0, admitted = 0, evicted = 0, rejected = 0, reserved = 0, filtered = 0,
+             erased = 0;
+};
+
+struct Table {
+    uint64_t num_buckets;
+    uint32_t dim;
+    bool dual;
+    uint64_t step = 1;                                   // R7
+    std::unordered_map<uint64_t, Bucket> buckets;       // created on first use
+    bool filtered = false;
+    std::unordered_set<uint64_t> filter;                // single mode only
+
+    uint64_t bucket1(uint64_t k) const { return murmur_fmix64(k) % num_buckets; }
+    uint64_t bucket2(uint64_t k) const {
+        uint64_t b1 = bucket1(k);
+        uint64_t b2 = murmur_fmix64(k ^ kDualSeed) % num_buckets;
+        if (b2 == b1) b2 = (b1 + 1) % num_buckets;
+        return b2;
+    }
+    bool simulated(uint64_t b) const { return !filtered || filter.count(b) != 0; }
+    Bucket& at(uint64_t b) { return buckets[b]; }
+
+    // Locate a resident key: returns bucket index and position, or false.
+    bool locate(uint64_t k, uint64_t* b_out, int* pos_out) {
+        uint64_t b1 = bucket1(k);
+        auto it = buckets.find(b1);
+        if (it != buckets.end()) {
+            int p = it->second.find(k);
+            if (p >= 0) { *b_out = b1; *pos_out = p; return true; }
+        }
+        if (dual) {
+            uint64_t b2 = bucket2(k);
+            auto it2 = buckets.find(b2);
+            if (it2 != buckets.end()) {
+                int p = it2->second.find(k);
+                if (p >= 0) { *b_out = b2; *pos_out = p; return true; }
+            }
+        }
+        return false;
+    }
+
+    void write_entry(Bucket& bk, int pos, uint64_t k, uint64_t s, const float* v) {
+        bk.keys[pos] = k;
+        bk.scores[pos] = s;
+        std::memcpy(&bk.values[static_cast<size_t>(pos) * dim], v, sizeof(float) * dim);
+    }
+    void append_entry(Bucket& bk, uint64_t k, uint64_t s, const float* v) {
+        bk.keys.push_back(k);
+        bk.scores.push_back(s);
+        bk.values.insert(bk.values.end(), v, v + dim);
+    }
+    void remove_entry(Bucket& bk, int pos) {
+        int last = bk.size() - 1;
+        if (pos != last) write_entry(bk, pos, bk.keys[last], bk.scores[last],
+                                     &bk.values[static_cast<size_t>(last) * dim]);
+        bk.keys.pop_back();
+        bk.scores.pop_back();
+        bk.values.resize(static_cast<size_t>(last) * dim);
+    }
+
+    // Outcome of one absent key (HKV Algorithm 2 / 3 return values).
+    enum Outcome { kInserted, kEvicted, kRejected };
+
+    // HKV Algorithm 2, branches after the (failed) lookup, on bucket b.
+    // On kEvicted, *victim receives the displaced key.
+    Outcome insert_single(uint64_t b, uint64_t k, uint64_t s, const float* v, uint64_t* victim) {
+        Bucket& bk = at(b);
+        if (bk.size() < kSlots) {                 // first empty slot exists
+            append_entry(bk, k, s, v);
+            return kInserted;
+        }
+        int m = bk.argmin_rank();                 // bucket full: eviction path
+        if (rank_less(s, k, bk.scores[m], bk.keys[m]))
+            return kRejected;                     // admission control
+        *victim = bk.keys[m];
+        write_entry(bk, m, k, s, v);              // replace the minimum
+        return kEvicted;
+    }
+
+    // HKV Algorithm 3 (score-based dual-bucket upsert), for an absent key.
+    Outcome insert_dual(uint64_t k, uint64_t s, const float* v, uint64_t* victim) {
+        uint64_t b1 = bucket1(k), b2 = bucket2(k);
+        Bucket& x = at(b1);
+        Bucket& y = at(b2);
+        if (x.size() < kSlots || y.size() < kSlots) {        // phase D1
+            Bucket& target = (y.size() < x.size()) ? y : x;  // less occupied, tie -> b1
+            append_entry(target, k, s, v);
+            return kInserted;
+        }
+        int m1 = x.argmin_rank(), m2 = y.argmin_rank();      // phase D2
+        bool pick2 = rank_less(y.scores[m2], y.keys[m2], x.scores[m1], x.keys[m1]);
+        Bucket& bs = pick2 ? y : x;
+        int m = pick2 ? m2 : m1;
+        if (!rank_less(bs.scores[m], bs.keys[m], s, k))      // admission control
+            return kRejected;
+        *victim = bs.keys[m];
+        write_entry(bs, m, k, s, v);
+        return kEvicted;
+    }
+
+    // Collapse a batch to the last occurrence of each valid key (R5) and
+    // return the surviving indices in batch order.
+    std::vector<uint64_t> last_occurrences(uint64_t n, const uint64_t* keys, Counts& c) {
+        std::unordered_map<uint64_t, uint64_t> last;
+        last.reserve(static_cast<size_t>(n) * 2 + 1);
+        for (uint64_t i = 0; i < n; ++i) {
+            if (is_reserved(keys[i])) { ++c.reserved; continue; }
+            last[keys[i]] = i;
+        }
+        std::vector<uint64_t> idx;
+        idx.reserve(last.size());
+        for (uint64_t i = 0; i < n; ++i)
+            if (!is_reserved(keys[i]) && last[keys[i]] == i) idx.push_back(i);
+        return idx;
+    }
+
+    bool skip_for_filter(uint64_t k, Counts& c) {
+        if (filtered && !simulated(bucket1(k))) { ++c.filtered; return true; }
+        return false;
+    }
+
+    Counts insert_or_assign(uint64_t n, const uint64_t* keys, const float* values,
+                            const uint64_t* scores) {
+        Counts c;
+        uint64_t step_score = step;
+        std::vector<uint64_t> idx = last_occurrences(n, keys, c);
+        std::vector<uint64_t> absent;
+        for (uint64_t i : idx) {                  // R6: resident keys first
+            uint64_t k = keys[i];
+            if (skip_for_filter(k, c)) continue;
+            uint64_t s = scores ? scores[i] : step_score;
+            uint64_t b; int p;
+            if (locate(k, &b, &p)) {              // HKV Algorithm 2, found branch
+                write_entry(at(b), p, k, s, values + i * dim);
+                ++c.updated;
+            } else {
+                absent.push_back(i);
+            }
+        }
+        // Then the absent keys, batch order.  The counts are batch-level and
+        // independent of the serial order: an absent key that is admitted and
+        // displaced again within the same call counts as rejected, and
+        // "evicted" counts only keys that were resident before the call.
+        std::unordered_set<uint64_t> admitted;
+        for (uint64_t i : absent) {
+            uint64_t k = keys[i];
+            uint64_t s = scores ? scores[i] : step_score;
+            uint64_t victim = 0;
+            Outcome o = dual ? insert_dual(k, s, values + i * dim, &victim)
+                             : insert_single(bucket1(k), k, s, values + i * dim, &victim);
+            if (o == kRejected) continue;
+            admitted.insert(k);
+            if (o == kEvicted) {
+                if (admitted.erase(victim) == 0) ++c.evicted;
+            }
+        }
+        c.admitted = admitted.size();
+        c.rejected = absent.size() - admitted.size();
+        if (!scores) ++step;
+        return c;
+    }
+
+    Counts assign(uint64_t n, const uint64_t* keys, const float* values, const uint64_t* scores) {
+        Counts c;
+        std::vector<uint64_t> idx = last_occurrences(n, keys, c);
+        for (uint64_t i : idx) {
+            uint64_t k = keys[i];
+            if (skip_for_filter(k, c)) continue;
+            uint64_t b; int p;
+            if (!locate(k, &b, &p)) continue;     // updater: absent keys are a no-op
+            Bucket& bk = at(b);
+            std::memcpy(&bk.values[static_cast<size_t>(p) * dim], values + i * dim,
+                        sizeof(float) * dim);
+            if (scores) bk.scores[p] = scores[i];
+            ++c.updated;
+        }
+        return c;
+    }
+
+    Counts erase(uint64_t n, const uint64_t* keys) {
+        Counts c;
+        for (uint64_t i = 0; i < n; ++i) {
+            uint64_t k = keys[i];
+            if (is_reserved(k)) { ++c.reserved; continue; }
+            if (skip_for_filter(k, c)) continue;
+            uint64_t b; int p;
+            if (!locate(k, &b, &p)) continue;
+            remove_entry(at(b), p);
+            ++c.erased;
+        }
+        return c;
+    }
+
+    // HKV Algorithm 1 (and its two-bucket form in dual mode): membership.
+    uint64_t find(uint64_t n, const uint64_t* keys, float* values_out, uint8_t* found_out,
+                  uint64_t* scores_out) {
+        uint64_t hits = 0;
+        for (uint64_t i = 0; i < n; ++i) {
+            uint64_t k = keys[i];
+            uint64_t b; int p;
+            if (is_reserved(k) || !locate(k, &b, &p)) { found_out[i] = 0; continue; }
+            Bucket& bk = at(b);
+            found_out[i] = 1;
+            std::memcpy(values_out + i * dim, &bk.values[static_cast<size_t>(p) * dim],
+                        sizeof(float) * dim);
+            if (scores_out) scores_out[i] = bk.scores[p];
+            ++hits;
+        }
+        return hits;
+    }
+
+    uint64_t size() const {
+        uint64_t s = 0;
+        for (const auto& kv : buckets) s += kv.second.keys.size();
+        return s;
+    }
+};
+
+struct Row { uint64_t key, score; const float* v; };
+
+}  // namespace
+
+extern "C" {
+
+struct oracle_counts {
+    uint64_t updated, admitted, evicted, rejected, reserved, filtered, erased;
+};
+
+static void put(const Counts& c, oracle_counts* out) {
+    if (!out) return;
+    out->updated = c.updated; out->admitted = c.admitted; out->evicted = c.evicted;
+    out->rejected = c.rejected; out->reserved = c.reserved; out->filtered = c.filtered;
+    out->erased = c.erased;
+}
+
+void* oracle_create(uint64_t num_buckets, uint32_t dim, int dual) {
+    if (num_buckets == 0 || dim == 0 || (dual && num_buckets < 2)) return nullptr;
+    Table* t = new Table();
+    t->num_buckets = num_buckets;
+    t->dim = dim;
+    t->dual = dual != 0;
+    return t;
+}
+
+void oracle_destroy(void* h) { delete static_cast<Table*>(h); }
+
+// Restrict the model to the listed buckets (single mode only); keys hashed
+// elsewhere are ignored and counted as "filtered".
+int oracle_set_bucket_filter(void* h, uint64_t n, const uint64_t* buckets) {
+    Table* t = static_cast<Table*>(h);
+    if (t->dual) return -1;
+    t->filtered = true;
+    t->filter.clear();
+    for (uint64_t i = 0; i < n; ++i) t->filter.insert(buckets[i]);
+    return 0;
+}
+
+uint64_t oracle_hash(uint64_t key) { return murmur_fmix64(key); }
+
+uint64_t oracle_bucket(void* h, uint64_t key, int which) {
+    Table* t = static_cast<Table*>(h);
+    return which == 0 ? t->bucket1(key) : t->bucket2(key);
+}
+
+void oracle_buckets(void* h, uint64_t n, const uint64_t* keys, int which, uint64_t* out) {
+    Table* t = static_cast<Table*>(h);
+    for (uint64_t i = 0; i < n; ++i) out[i] = which == 0 ? t->bucket1(keys[i]) : t->bucket2(keys[i]);
+}
+
+uint64_t oracle_step(void* h) { return static_cast<Table*>(h)->step; }
+
+void oracle_insert_or_assign(void* h, uint64_t n, const uint64_t* keys, const float* values,
+                             const uint64_t* scores, oracle_counts* out) {
+    put(static_cast<Table*>(h)->insert_or_assign(n, keys, values, scores), out);
+}
+
+void oracle_assign(void* h, uint64_t n, const uint64_t* keys, const float* values,
+                   const uint64_t* scores, oracle_counts* out) {
+    put(static_cast<Table*>(h)->assign(n, keys, values, scores), out);
+}
+
+void oracle_erase(void* h, uint64_t n, const uint64_t* keys, oracle_counts* out) {
+    put(static_cast<Table*>(h)->erase(n, keys), out);
+}
+
+uint64_t oracle_find(void* h, uint64_t n, const uint64_t* keys, float* values_out,
+                     uint8_t* found_out, uint64_t* scores_out) {
+    return static_cast<Table*>(h)->find(n, keys, values_out, found_out, scores_out);
+}
+
+uint64_t oracle_size(void* h) { return static_cast<Table*>(h)->size(); }
+
+uint64_t oracle_bucket_size(void* h, uint64_t b) {
+    Table* t = static_cast<Table*>(h);
+    auto it = t->buckets.find(b);
+    return it == t->buckets.end() ? 0 : it->second.keys.size();
+}
+
+// Entries of buckets [b_begin, b_end) whose score is >= min_score, sorted by
+// key.  Pass NULL outputs to only count.  Returns the number of entries.
+uint64_t oracle_export(void* h, uint64_t b_begin, uint64_t b_end, uint64_t min_score,
+                       uint64_t* keys_out, float* values_out, uint64_t* scores_out) {
+    Table* t = static_cast<Table*>(h);
+    std::vector<Row> rows;
+    for (auto& kv : t->buckets) {
+        if (kv.first < b_begin || kv.first >= b_end) continue;
+        const Bucket& bk = kv.second;
+        for (int i = 0; i < bk.size(); ++i)
+            if (bk.scores[i] >= min_score)
+                rows.push_back({bk.keys[i], bk.scores[i], &bk.values[static_cast<size_t>(i) * t->dim]});
+    }
+    std::sort(rows.begin(), rows.end(), [](const Row& a, const Row& b) { return a.key < b.key; });
+    for (size_t i = 0; i < rows.size(); ++i) {
+        if (keys_out) keys_out[i] = rows[i].key;
+        if (scores_out) scores_out[i] = rows[i].score;
+        if (values_out) std::memcpy(values_out + i * t->dim, rows[i].v, sizeof(float) * t->dim);
+    }
+    return rows.size();
+}
+
+}  // extern "C"
