@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark: batched find + insert_or_assign on the cache-semantic GPU hash
+table, single-bucket mode, capacity 2^22 slots, dim 32 (float32 values),
+batches of 2^20 keys at an 80% hit rate, load factor swept 0.50 -> 1.00.
+
+One step = one insert_or_assign batch (80% resident keys, 20% fresh, scored
+by the step counter) followed by one find batch (80% resident, 20% fresh) on
+the full table (load factor 1.00).  `value` = keys processed per second over
+the timed steps (both batches), in billions (B-KV/s).  Inputs are resident
+in HBM; L2 is flushed (256 MiB write) between steps, outside the timed events.
+
+Also reported: the per-load-factor find and upsert throughput, the roofline
+of the dominant kernel against the measured HBM peak, the oracle (CPU) on a
+bounded sample, end-to-end throughput with host buffers, and SM clocks.
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
+and its own key stream (no collective on the data path); timing is the max
+over ranks and `value` sums the keys of all ranks.
+
+`--impl reference` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "find / insert_or_assign B-KV/s vs load factor 0.5–1.0; % of HBM roofline"
+CAP, DIM, BATCH, FILL_BATCH, HIT = 1 << 22, 32, 1 << 20, 1 << 16, 0.8
+LAMBDAS = (0.5, 0.75, 0.9, 1.0)
+WORKLOAD = "single-bucket, capacity 2^22, dim 32 f32, batch 2^20, 80% hits, step scores"
+
+
+def find_bytes_per_key(dim, hit):
+    """Algorithmic bytes of one find (Algorithm 1): key 8, digest line 128,
+    expected key confirms 8*(1 + 127/256) on a hit or 8*128/256 on a miss,
+    value row read + output row write 2*4*dim, found flag 1, score read +
+    write 16 (hits, scores requested)."""
+    d = 4 * dim
+    return hit * (8 + 128 + 8 * (1 + 127 / 256) + 2 * d + 1 + 16) + (1 - hit) * (8 + 128 + 4 + 1)
+
+
+def upsert_bytes(n_keys, dim, n_buckets_touched, n_buckets_scanned, n_rows_written, with_scores):
+    """Algorithmic bytes of one bucket-owner upsert call: per key the input
+    key, value row and score (8 + 4*dim + 8*with_scores); per touched bucket
+    its 128 keys read and written back (2 KiB) and its digest line written
+    (128); per bucket that needed an eviction decision its 128 scores read and
+    written back (2 KiB); per final new occupant one value row written."""
+    d = 4 * dim
+    return (n_keys * (8 + d + 8 * with_scores) + n_buckets_touched * (2048 + 128)
+            + n_buckets_scanned * 2048 + n_rows_written * d)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.window = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "10"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)  # let the sampler start before the timed region
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def mark(self, t0, t1):
+        """Wall-clock bounds of the timed region."""
+        self.window = (t0, t1)
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        import datetime
+        rows = []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2].split()[0]), float(parts[3].split()[0]),
+                             [nm for nm, v in zip(names, parts[6:10]) if v.lower() == "active"]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sel = rows
+        if self.window:
+            a, b = self.window
+            sel = [r for r in rows if a - 0.02 <= r[0] <= b + 0.02]
+            if not sel:  # region shorter than the sampling period: nearest samples
+                mid = (a + b) / 2
+                sel = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+        reasons = sorted({x for r in sel for x in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import hash_table_cache_gb300 as hkv
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    hkv.load()
+    seed_base = 1000 * rank
+
+    def dk(a):
+        return torch.from_numpy(wl.as_i64(a)).to(dev)
+
+    def fill(t, target, pos, keys):
+        while t.size() < target and pos < keys.size:
+            k = keys[pos:pos + FILL_BATCH]
+            t.insert_or_assign(dk(k), wl.key_values_torch(dk(k), DIM, salt=1), None)
+            pos += FILL_BATCH
+        return pos
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) * 1e-3
+
+    keys = wl.unique_keys(3 + seed_base, 2 * CAP)
+    sweep = {}
+    lambdas = () if args.skip_sweep else LAMBDAS
+    # load-factor sweep: find on the filling table; upsert on a re-filled table
+    t = hkv.HashTable(CAP, DIM, device=local)
+    pos = 0
+    for lam in lambdas:
+        pos = fill(t, lam * CAP, pos, keys)
+        res, _, _ = t.export(with_values=False)
+        res = res.cpu().numpy().view(np.uint64)
+        q, _ = wl.hit_mix(4 + seed_base, res, 5 + seed_base, BATCH, HIT)
+        qd = dk(q)
+        vout = torch.empty((BATCH, DIM), dtype=torch.float32, device=dev)
+        fout = torch.empty(BATCH, dtype=torch.uint8, device=dev)
+        sout = torch.empty(BATCH, dtype=torch.int64, device=dev)
+        for _ in range(2):
+            t.find(qd, vout, fout, sout)
+        ft = [timed(lambda: t.find(qd, vout, fout, sout)) for _ in range(5)]
+        sweep[lam] = {"lambda_actual": t.size() / CAP, "find_bkvs": BATCH / statistics.median(ft) / 1e9,
+                      "find_hit_rate": float(fout.float().mean().item())}
+    t.close()
+    for lam in lambdas:
+        ut = []
+        for rep in range(3):
+            t = hkv.HashTable(CAP, DIM, device=local)
+            fill(t, lam * CAP, 0, keys)
+            res, _, _ = t.export(with_values=False)
+            res = res.cpu().numpy().view(np.uint64)
+            q, _ = wl.hit_mix(6 + seed_base + rep, res, 7 + seed_base + rep, BATCH, HIT)
+            qd = dk(q)
+            vd = wl.key_values_torch(qd, DIM, salt=2)
+            ut.append(timed(lambda: t.insert_or_assign(qd, vd, None)))
+            t.close()
+        sweep[lam]["upsert_bkvs"] = BATCH / statistics.median(ut) / 1e9
+
+    # headline: steps at load factor 1.0
+    t = hkv.HashTable(CAP, DIM, device=local)
+    fill(t, CAP, 0, keys)
+    res, _, _ = t.export(with_values=False)
+    res = res.cpu().numpy().view(np.uint64)
+    nsteps = args.warmup + args.steps
+    up_k, up_v, fq = [], [], []
+    for s in range(nsteps):
+        q, _ = wl.hit_mix(100 + s + seed_base, res, 200 + seed_base, BATCH, HIT, fresh_start=s * BATCH)
+        qd = dk(q)
+        up_k.append(qd)
+        up_v.append(wl.key_values_torch(qd, DIM, salt=3 + s))
+        # find: 80% drawn from the keys this step's upsert just wrote (resident
+        # after it: they carry the newest score), 20% fresh
+        f, _ = wl.hit_mix(300 + s + seed_base, q, 400 + seed_base, BATCH, HIT, fresh_start=s * BATCH)
+        fq.append(dk(f))
+    vout = torch.empty((BATCH, DIM), dtype=torch.float32, device=dev)
+    fout = torch.empty(BATCH, dtype=torch.uint8, device=dev)
+    sout = torch.empty(BATCH, dtype=torch.int64, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsteps)]
+    torch.cuda.synchronize()
+    for s in range(args.warmup):
+        flush.zero_()
+        t.insert_or_assign(up_k[s], up_v[s], None)
+        t.find(fq[s], vout, fout, sout)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t.reset_op_counts()
+    with Clocks(local) as clk:
+        w0 = time.time()
+        for s in range(args.warmup, nsteps):
+            flush.zero_()
+            e0, e1, e2 = ev[s]
+            e0.record(stream)
+            t.insert_or_assign(up_k[s], up_v[s], None)
+            e1.record(stream)
+            t.find(fq[s], vout, fout, sout)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        clk.mark(w0, time.time())
+    if world > 1:
+        dist.barrier()
+    up_t = [ev[s][0].elapsed_time(ev[s][1]) * 1e-3 for s in range(args.warmup, nsteps)]
+    fi_t = [ev[s][1].elapsed_time(ev[s][2]) * 1e-3 for s in range(args.warmup, nsteps)]
+    total = sum(up_t) + sum(fi_t)
+    counts = t.op_counts()
+    if world > 1:
+        tt = torch.tensor([total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total = float(tt.item())
+    keys_done = 2 * BATCH * args.steps * world
+    value = keys_done / total / 1e9
+
+    # roofline of the dominant kernel
+    peak, peak_kind = read_peaks()
+    hit_rate = float(fout.float().mean().item())
+    f_avg, u_avg = statistics.mean(fi_t), statistics.mean(up_t)
+    fb = find_bytes_per_key(DIM, hit_rate) * BATCH
+    n_upd = counts["updated"] / args.steps
+    scanned = CAP // 128  # every bucket receives fresh keys at this batch size
+    ub = upsert_bytes(BATCH, DIM, CAP // 128, scanned,
+                      (counts["updated"] + counts["admitted"]) / args.steps, False)
+    find_roof = {"bound": "hbm", "achieved": fb / f_avg / 1e9, "peak": peak, "unit": "GB/s",
+                 "frac": fb / f_avg / 1e9 / peak, "traffic": None, "kernel": "find_kernel",
+                 "bytes_per_launch": fb, "avg_launch_s": f_avg, "peak_kind": peak_kind}
+    up_roof = {"bound": "hbm", "achieved": ub / u_avg / 1e9, "peak": peak, "unit": "GB/s",
+               "frac": ub / u_avg / 1e9 / peak, "traffic": None, "kernel": "insert_or_assign (call)",
+               "bytes_per_launch": ub, "avg_launch_s": u_avg, "peak_kind": peak_kind}
+    dominant = find_roof if f_avg >= u_avg else up_roof
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hk = [up_k[s].cpu().pin_memory() for s in range(2)]
+        hv = [up_v[s].cpu().pin_memory() for s in range(2)]
+        hq = [fq[s].cpu().pin_memory() for s in range(2)]
+        dkk = torch.empty_like(up_k[0]); dvv = torch.empty_like(up_v[0]); dqq = torch.empty_like(fq[0])
+        hvo = torch.empty((BATCH, DIM), dtype=torch.float32).pin_memory()
+        hfo = torch.empty(BATCH, dtype=torch.uint8).pin_memory()
+        hso = torch.empty(BATCH, dtype=torch.int64).pin_memory()
+        e_t = []
+        for s in range(4):
+            i = s % 2
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dkk.copy_(hk[i], non_blocking=True); dvv.copy_(hv[i], non_blocking=True)
+            dqq.copy_(hq[i], non_blocking=True)
+            t.insert_or_assign(dkk, dvv, None)
+            t.find(dqq, vout, fout, sout)
+            hvo.copy_(vout, non_blocking=True); hfo.copy_(fout, non_blocking=True)
+            hso.copy_(sout, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if s >= 1:
+                e_t.append(a.elapsed_time(b) * 1e-3)
+        bi = hk[0].numel() * 8 + hv[0].numel() * 4 + hq[0].numel() * 8
+        bo = hvo.numel() * 4 + hfo.numel() + hso.numel() * 8
+        e2e = {"value": 2 * BATCH * world / statistics.mean(e_t) / 1e9, "unit": "B-KV/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    t.close()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "B-KV/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u64 keys/scores, f32 values (copied)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "capacity": CAP, "dim": DIM, "batch": BATCH,
+                   "hit_rate": HIT, "load_factor": 1.0, "mode": "single",
+                   "l2": "flushed between steps (256 MiB write), flush outside timed events",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": dominant,
+        "roofline_all": {"find": find_roof, "insert_or_assign": up_roof},
+        "per_step": {"insert_or_assign_s": statistics.mean(up_t), "find_s": statistics.mean(fi_t),
+                     "find_bkvs": BATCH / f_avg / 1e9, "upsert_bkvs": BATCH / u_avg / 1e9,
+                     "find_hit_rate": hit_rate, "op_counts": counts},
+        "lambda_sweep": {str(k): v for k, v in sweep.items()},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": args.steps * (6 + 1),
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline, and the --impl reference arm)
+# ---------------------------------------------------------------------------
+SAMPLE_EVERY = 8  # the oracle simulates every 8th bucket of the table
+
+
+def oracle_step_rate(seconds_budget, steps=None):
+    """Run the oracle on a bounded sample of the same workload: the buckets b
+    with b % 8 == 0 of the 2^22-slot table (filled to load factor 1.0 with the
+    same key stream), then steps of (insert_or_assign 2^20, find 2^20) at 80%%
+    hits restricted to the keys of those buckets.  Returns (keys/s, steps,
+    step times, keys per step)."""
+    import oracle
+    nb = CAP // 128
+    o = oracle.OracleTable(nb, DIM)
+    o.set_bucket_filter(np.arange(0, nb, SAMPLE_EVERY, dtype=np.uint64))
+    keys = wl.unique_keys(3, 2 * CAP)
+
+    def sampled(k):
+        return k[o.buckets_of(k) % np.uint64(SAMPLE_EVERY) == 0]
+
+    pos = 0
+    while o.size() < CAP // SAMPLE_EVERY and pos < keys.size:
+        k = sampled(keys[pos:pos + FILL_BATCH])
+        o.insert_or_assign(k, wl.key_values(k, DIM, salt=1), None)
+        pos += FILL_BATCH
+    res = o.export()[0]
+    times, nkeys = [], []
+    s = 0
+    t_start = time.perf_counter()
+    while True:
+        # the full batch restricted to the sampled buckets: 1/8 of the hits
+        # (drawn from the residents) and the fresh keys that land there
+        m = BATCH // SAMPLE_EVERY
+        q = np.concatenate([wl.choice(100 + s, res, int(HIT * m)),
+                            sampled(wl.unique_keys(200, int((1 - HIT) * BATCH), s * BATCH))])
+        q = q[wl.permutation(150 + s, q.size)]
+        v = wl.key_values(q, DIM, salt=3 + s)
+        f = np.concatenate([wl.choice(300 + s, q, int(HIT * m)),
+                            sampled(wl.unique_keys(400, int((1 - HIT) * BATCH), s * BATCH))])
+        a = time.perf_counter()
+        o.insert_or_assign(q, v, None)
+        o.find(f)
+        times.append(time.perf_counter() - a)
+        nkeys.append(q.size + f.size)
+        s += 1
+        if steps is not None and s >= steps:
+            break
+        if steps is None and time.perf_counter() - t_start > seconds_budget:
+            break
+    return sum(nkeys) / sum(times), len(times), times, nkeys
+
+
+def cpu_baseline(seconds):
+    rate, n, _, nk = oracle_step_rate(seconds)
+    return {"value": rate / 1e9, "unit": "B-KV/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} step(s) of insert_or_assign + find restricted to every "
+                      f"{SAMPLE_EVERY}th bucket of the 2^22-slot table at load factor 1.0 "
+                      f"(~{int(statistics.mean(nk))} keys per step; fill untimed), single-threaded"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    rate, n, times, nk = oracle_step_rate(None, steps=args.warmup + args.steps)
+    w = args.warmup if len(times) > args.warmup else 0
+    timed, tk = times[w:], nk[w:]
+    value = sum(tk) / sum(timed) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "B-KV/s", "n_gpus": world, "steps": len(timed),
+        "warmup": args.warmup, "ms_per_step": sum(timed) / len(timed) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u64 keys/scores, f32 values (copied)", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD, "capacity": CAP, "dim": DIM, "batch": BATCH,
+                   "hit_rate": HIT, "load_factor": 1.0, "mode": "single",
+                   "parallelism": "cpu, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": "B-KV/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(timed)} timed step(s) of insert_or_assign + find "
+                                   f"restricted to every {SAMPLE_EVERY}th bucket of the 2^22-slot "
+                                   f"table at load factor 1.0 (~{int(statistics.mean(tk))} keys/step)"},
+        "e2e": {"value": value, "unit": "B-KV/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-sweep", action="store_true", help="only the headline steps")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+// common.cuh -- table layout, hashing and small device helpers shared by the
+// kernels of the library.
+//
+// Layout in HBM (HierarchicalKV §3.2 Figure 4, §3.6, §4.2): structure of
+// arrays over B buckets of 128 slots; slot j of bucket b is row r = b*128 + j.
+//   digests[B*128]  uint8   one 128-byte line per bucket, 0 = free slot
+//   keys[B*128]     uint64  EMPTY_KEY marks a free slot
+//   scores[B*128]   uint64
+//   values          float32 rows of `dim`; rows < hbm_rows in HBM, the rest in
+//                   mapped pinned host memory (tiered mode)
+// No per-entry pointer is stored: a value row is found from (bucket, slot).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace hkv {
+
+constexpr int kSlots = 128;
+constexpr uint64_t kEmptyKey = 0xFFFFFFFFFFFFFFFFull;
+constexpr uint64_t kReservedLo = 0xFFFFFFFFFFFFFFF0ull;
+constexpr uint64_t kDualSeed = 0x9E3779B97F4A7C15ull;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+
+// Device-resident counters of one table.  Fields are updated with atomics.
+struct DeviceStats {
+  unsigned long long reserved;   // reserved keys skipped
+  unsigned long long timeouts;   // keys abandoned after a bounded lock wait
+  unsigned long long updated;
+  unsigned long long admitted;
+  unsigned long long evicted;
+  unsigned long long rejected;
+  unsigned long long erased;
+  unsigned long long size;       // resident entries
+  unsigned long long fills;      // dual mode: entries placed in free slots by the current call
+};
+
+// Everything a kernel needs to address the table; passed by value.
+struct TableView {
+  uint8_t* digests;
+  uint64_t* keys;
+  uint64_t* scores;
+  float* values_hbm;
+  float* values_host;     // device pointer of the mapped host slab, or null
+  uint64_t hbm_rows;      // rows below this index live in values_hbm
+  uint64_t num_buckets;
+  uint64_t bucket_mask;   // num_buckets - 1 when a power of two, else 0
+  uint32_t dim;
+  uint32_t dual;
+  uint32_t* locks;        // dual mode: one word per bucket
+  DeviceStats* stats;
+};
+
+// H(k): the 64-bit MurmurHash3 finalizer (HKV §3.1 names a Murmur3-derived
+// hash; the finalizer is the published 64-bit mixing step).
+__host__ __device__ __forceinline__ uint64_t hash64(uint64_t h) {
+  h ^= h >> 33;
+  h *= 0xff51afd7ed558ccdull;
+  h ^= h >> 33;
+  h *= 0xc4ceb9fe1a85ec53ull;
+  h ^= h >> 33;
+  return h;
+}
+
+__host__ __device__ __forceinline__ uint64_t bucket_of_hash(const TableView& t, uint64_t h) {
+  return t.bucket_mask ? (h & t.bucket_mask) : (h % t.num_buckets);
+}
+
+// Second candidate bucket for dual mode (HKV §3.4, "two candidate buckets via
+// independent hashes"); never equal to the first.
+__host__ __device__ __forceinline__ uint64_t bucket2_of(const TableView& t, uint64_t key,
+                                                        uint64_t b1) {
+  uint64_t b2 = bucket_of_hash(t, hash64(key ^ kDualSeed));
+  if (b2 == b1) b2 = (b1 + 1 == t.num_buckets) ? 0 : b1 + 1;
+  return b2;
+}
+
+// 8-bit digest from bits 32..39 of the hash (HKV §3.2).  Byte 0 is kept for
+// free slots, so a digest of 0 is stored as 1.
+__host__ __device__ __forceinline__ uint32_t digest_of_hash(uint64_t h) {
+  uint32_t d = static_cast<uint32_t>(h >> 32) & 0xFFu;
+  return d ? d : 1u;
+}
+
+__device__ __forceinline__ bool is_reserved(uint64_t k) { return k >= kReservedLo; }
+
+__device__ __forceinline__ float* row_ptr(const TableView& t, uint64_t row) {
+  return row < t.hbm_rows ? t.values_hbm + row * t.dim
+                          : t.values_host + (row - t.hbm_rows) * t.dim;
+}
+
+// ---------------------------------------------------------------------------
+// Memory access helpers (inline PTX for the cache hints).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+// Streaming read: no L1 allocation (value rows are touched once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+// Streaming store (evict-first), for output rows and written value rows.
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_nc_u64(const uint64_t* p) {
+  uint64_t r;
+  asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(r) : "l"(p));
+  return r;
+}
+// L2-coherent loads (bypass L1) for data other blocks may have written in
+// the same kernel.
+__device__ __forceinline__ uint64_t ld_cg_u64(const uint64_t* p) {
+  uint64_t r;
+  asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(r) : "l"(p) : "memory");
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+
+// Exact per-byte equality mask: bit i of the result is set when byte i of
+// `w` equals byte i of `pat` (i = 0..3).  Branch-free SWAR test for a zero
+// byte in w ^ pat.
+__device__ __forceinline__ uint32_t byte_eq_mask4(uint32_t w, uint32_t pat) {
+  uint32_t x = w ^ pat;
+  uint32_t y = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x;  // high bit set iff byte != 0
+  uint32_t z = ~y & 0x80808080u;                      // high bit set iff byte == 0
+  return ((z >> 7) & 1u) | ((z >> 14) & 2u) | ((z >> 21) & 4u) | ((z >> 28) & 8u);
+}
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+// Warp-aggregated atomic add of a per-lane contribution (any lane set).
+__device__ __forceinline__ void warp_add(unsigned long long* p, unsigned long long v) {
+  unsigned long long s = v;
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  if (lane_id() == 0 && s) atomicAdd(p, s);
+}
+
+// Copy one value row of `dim` floats with the 8 lanes of a tile: lane `sub`
+// (0..7) moves 16-byte chunks sub, sub+8, ...  `vec` selects the 16-byte path
+// (both rows 16-byte aligned and dim % 4 == 0); otherwise 4-byte words.
+__device__ __forceinline__ void tile_copy_row(float* dst, const float* src, uint32_t dim,
+                                              unsigned sub, bool vec, bool stream_store) {
+  if (vec) {
+    const uint32_t chunks = dim >> 2;
+    for (uint32_t c = sub; c < chunks; c += 8) {
+      uint4 v = ld_stream_v4(src + 4 * c);
+      if (stream_store) st_stream_v4(dst + 4 * c, v);
+      else *reinterpret_cast<uint4*>(dst + 4 * c) = v;
+    }
+  } else {
+    for (uint32_t c = sub; c < dim; c += 8) dst[c] = src[c];
+  }
+}
+
+// Probe bucket b for `key` with the 8 lanes of a tile (HKV Algorithm 1):
+// lane `sub` loads 16 bytes of the 128-byte digest line, byte-compares them
+// with the key's digest (`pat` = digest * 0x01010101) and confirms each match
+// with an 8-byte key load.  Returns the slot, or -1; uniform across the tile.
+// kNC selects read-only loads, legal only when no thread of the running
+// kernel writes keys or digests.
+template <bool kNC>
+__device__ __forceinline__ int tile_probe(const TableView& t, uint64_t b, uint64_t key, uint32_t pat,
+                                          unsigned sub, unsigned tmask) {
+  const uint8_t* dp = t.digests + b * kSlots + sub * 16;
+  uint4 dg;
+  if (kNC) dg = ld_nc_v4(dp);
+  else dg = ld_cg_v4(dp);
+  uint32_t m = byte_eq_mask4(dg.x, pat) | (byte_eq_mask4(dg.y, pat) << 4) |
+               (byte_eq_mask4(dg.z, pat) << 8) | (byte_eq_mask4(dg.w, pat) << 12);
+  int hit = -1;
+  const uint64_t* kb = t.keys + b * kSlots + sub * 16;
+  while (m) {
+    const int bit = __ffs(m) - 1;
+    m &= m - 1;
+    const uint64_t k = kNC ? ld_nc_u64(kb + bit) : ld_cg_u64(kb + bit);
+    if (k == key) {
+      hit = static_cast<int>(sub * 16 + bit);
+      break;
+    }
+  }
+  const unsigned bal = __ballot_sync(tmask, hit >= 0) & tmask;
+  if (!bal) return -1;
+  return __shfl_sync(tmask, hit, __ffs(bal) - 1);
+}
+
+}  // namespace hkv

@@ -1,0 +1,54 @@
+// launch.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace hkv {
+
+// Scratch of one insert_or_assign / assign call (device memory, call-owned).
+struct UpsertScratch {
+  uint64_t* map_keys;   // dedup map, map_size entries, EMPTY-initialised
+  uint32_t* map_idx;    // last batch index + 1 per map entry, 0-initialised
+  uint32_t map_size;    // power of two
+  uint32_t* bkt;        // per key: its bucket if it is a last occurrence, else kNone
+  uint32_t* rnk;        // per key: position inside its bucket group
+  uint32_t* cnt;        // per bucket: group size (0-initialised)
+  uint32_t* off;        // per bucket: group start in `group`
+  uint32_t* group;      // batch indices grouped by bucket
+  uint32_t* cursor;     // bump allocator for group starts / miss list length (0-initialised)
+};
+
+// Bytes of scratch an insert_or_assign / assign of n keys needs, and the
+// carving of one allocation into the UpsertScratch arrays.
+size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, bool need_groups);
+UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, bool need_groups);
+// Enqueue the clears the scratch needs before use.
+cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, bool need_groups,
+                                 cudaStream_t st);
+
+cudaError_t launch_find(const TableView& t, uint64_t n, const uint64_t* keys, float* values_out,
+                        uint8_t* found_out, uint64_t* scores_out, cudaStream_t st);
+
+cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
+                          const uint64_t* keys, const float* values, const uint64_t* scores,
+                          uint64_t step_score, cudaStream_t st);
+
+cudaError_t launch_assign(const TableView& t, const UpsertScratch& s, uint64_t n,
+                          const uint64_t* keys, const float* values, const uint64_t* scores,
+                          cudaStream_t st);
+
+cudaError_t launch_erase(const TableView& t, uint64_t n, const uint64_t* keys, cudaStream_t st);
+
+cudaError_t launch_export(const TableView& t, uint64_t slot_begin, uint64_t slot_end,
+                          uint64_t min_score, uint64_t* keys_out, float* values_out,
+                          uint64_t* scores_out, uint64_t* count_out, cudaStream_t st);
+
+cudaError_t launch_clear_table(const TableView& t, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace hkv

@@ -1,0 +1,420 @@
+// table.cu -- the C ABI (include/hkv.h): table construction, argument
+// checking, scratch management and reader/updater/inserter ordering.
+//
+// Role ordering (HierarchicalKV §3.5 Table 4, §4.4): the paper mirrors three
+// host atomic counters to the device with a one-thread kernel.  Here every
+// call records a CUDA event on its stream and makes its stream wait, in host
+// issue order, for the events of the earlier calls whose role conflicts with
+// its own: readers wait for updaters and inserters, updaters for readers and
+// inserters, inserters for everyone.  Compatible calls on different streams
+// overlap; nothing spins on the device.
+#include <cstddef>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "hkv.h"
+#include "launch.h"
+
+namespace {
+
+enum class Role { kReader, kUpdater, kInserter };
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) == cudaSuccess && cur != dev) {
+      prev = cur;
+      cudaSetDevice(dev);
+    }
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+// Events of the calls issued since the last inserter, by role.
+class RoleTracker {
+ public:
+  cudaError_t before(Role r, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (last_inserter_) e = cudaStreamWaitEvent(s, last_inserter_, 0);
+    if (e == cudaSuccess && r != Role::kUpdater)
+      for (cudaEvent_t ev : updaters_)
+        if ((e = cudaStreamWaitEvent(s, ev, 0)) != cudaSuccess) break;
+    if (e == cudaSuccess && r != Role::kReader)
+      for (cudaEvent_t ev : readers_)
+        if ((e = cudaStreamWaitEvent(s, ev, 0)) != cudaSuccess) break;
+    return e;
+  }
+
+  cudaError_t after(Role r, cudaStream_t s, cudaStream_t aux) {
+    cudaEvent_t ev = nullptr;
+    cudaError_t e = get(&ev);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) return e;
+    if (r == Role::kInserter) {
+      if (last_inserter_) free_.push_back(last_inserter_);
+      for (cudaEvent_t x : readers_) free_.push_back(x);
+      for (cudaEvent_t x : updaters_) free_.push_back(x);
+      readers_.clear();
+      updaters_.clear();
+      last_inserter_ = ev;
+      return cudaSuccess;
+    }
+    std::vector<cudaEvent_t>& list = (r == Role::kReader) ? readers_ : updaters_;
+    list.push_back(ev);
+    if (list.size() > 16) return join(list, aux);
+    return cudaSuccess;
+  }
+
+  // Block the host until every recorded call has finished.
+  cudaError_t wait_all() {
+    cudaError_t e = cudaSuccess;
+    if (last_inserter_) e = cudaEventSynchronize(last_inserter_);
+    for (cudaEvent_t x : readers_)
+      if (e == cudaSuccess) e = cudaEventSynchronize(x);
+    for (cudaEvent_t x : updaters_)
+      if (e == cudaSuccess) e = cudaEventSynchronize(x);
+    return e;
+  }
+
+  void destroy() {
+    if (last_inserter_) cudaEventDestroy(last_inserter_);
+    for (cudaEvent_t x : readers_) cudaEventDestroy(x);
+    for (cudaEvent_t x : updaters_) cudaEventDestroy(x);
+    for (cudaEvent_t x : free_) cudaEventDestroy(x);
+    last_inserter_ = nullptr;
+    readers_.clear();
+    updaters_.clear();
+    free_.clear();
+  }
+
+ private:
+  cudaError_t get(cudaEvent_t* ev) {
+    if (!free_.empty()) {
+      *ev = free_.back();
+      free_.pop_back();
+      return cudaSuccess;
+    }
+    return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  }
+
+  // Replace a long list by one event that completes after all of them.
+  cudaError_t join(std::vector<cudaEvent_t>& list, cudaStream_t aux) {
+    cudaError_t e = cudaSuccess;
+    for (cudaEvent_t x : list)
+      if ((e = cudaStreamWaitEvent(aux, x, 0)) != cudaSuccess) return e;
+    cudaEvent_t j = nullptr;
+    if ((e = get(&j)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(j, aux)) != cudaSuccess) return e;
+    for (cudaEvent_t x : list) free_.push_back(x);
+    list.assign(1, j);
+    return cudaSuccess;
+  }
+
+  cudaEvent_t last_inserter_ = nullptr;
+  std::vector<cudaEvent_t> readers_, updaters_, free_;
+};
+
+hkv_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return HKV_OK;
+  if (e == cudaErrorMemoryAllocation) return HKV_ERR_OOM;
+  return HKV_ERR_CUDA;
+}
+
+}  // namespace
+
+struct hkv_table {
+  hkv::TableView v{};
+  int device = 0;
+  uint32_t mode = 0;
+  uint64_t capacity = 0;
+  float* host_slab = nullptr;  // host address of the mapped value slab
+  cudaMemPool_t pool = nullptr;
+  cudaStream_t aux = nullptr;
+  uint64_t step = 1;
+  RoleTracker roles;
+  std::mutex mu;
+};
+
+namespace {
+
+void release(hkv_table* t) {
+  if (!t) return;
+  DeviceGuard g(t->device);
+  t->roles.wait_all();
+  t->roles.destroy();
+  if (t->aux) cudaStreamDestroy(t->aux);
+  if (t->pool) cudaMemPoolDestroy(t->pool);
+  cudaFree(t->v.digests);
+  cudaFree(t->v.keys);
+  cudaFree(t->v.scores);
+  cudaFree(t->v.values_hbm);
+  cudaFree(t->v.locks);
+  cudaFree(t->v.stats);
+  if (t->host_slab) cudaFreeHost(t->host_slab);
+  delete t;
+}
+
+bool batch_ok(hkv_table* t, uint64_t n) { return t && n <= HKV_MAX_BATCH; }
+
+// Common frame of a batched call: lock, select the device, order by role,
+// run `body`, record the role event.
+template <class F>
+hkv_status run_call(hkv_table* t, Role r, void* stream, F&& body) {
+  std::lock_guard<std::mutex> lk(t->mu);
+  DeviceGuard g(t->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = t->roles.before(r, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  hkv_status st = body(s);
+  e = t->roles.after(r, s, t->aux);
+  if (st != HKV_OK) return st;
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t value_hbm_bytes,
+                      int device, hkv_table** out) {
+  if (!out) return HKV_ERR_INVALID;
+  *out = nullptr;
+  if (capacity == 0 || capacity % hkv::kSlots != 0 || dim == 0) return HKV_ERR_INVALID;
+  if (mode & ~static_cast<uint32_t>(HKV_MODE_DUAL | HKV_MODE_TIERED)) return HKV_ERR_INVALID;
+  const uint64_t nb = capacity / hkv::kSlots;
+  if (nb >= 0xFFFFFFFFull) return HKV_ERR_INVALID;
+  const bool dual = (mode & HKV_MODE_DUAL) != 0;
+  if (dual && nb < 2) return HKV_ERR_INVALID;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+    return HKV_ERR_INVALID;
+
+  hkv_table* t = new (std::nothrow) hkv_table();
+  if (!t) return HKV_ERR_OOM;
+  t->device = device;
+  t->mode = mode;
+  t->capacity = capacity;
+  DeviceGuard g(device);
+
+  uint64_t hbm_rows = capacity;
+  if (mode & HKV_MODE_TIERED) {
+    const uint64_t bucket_bytes = static_cast<uint64_t>(hkv::kSlots) * 4ull * dim;
+    const uint64_t hb = value_hbm_bytes / bucket_bytes;
+    hbm_rows = (hb < nb ? hb : nb) * hkv::kSlots;
+  }
+  hkv::TableView& v = t->v;
+  v.num_buckets = nb;
+  v.bucket_mask = (nb & (nb - 1)) == 0 ? nb - 1 : 0;
+  v.dim = dim;
+  v.dual = dual ? 1u : 0u;
+  v.hbm_rows = hbm_rows;
+
+  cudaError_t e = cudaMalloc(&v.digests, capacity);
+  if (e == cudaSuccess) e = cudaMalloc(&v.keys, capacity * 8);
+  if (e == cudaSuccess) e = cudaMalloc(&v.scores, capacity * 8);
+  if (e == cudaSuccess) e = cudaMalloc(&v.stats, sizeof(hkv::DeviceStats));
+  if (e == cudaSuccess && hbm_rows) e = cudaMalloc(&v.values_hbm, hbm_rows * 4ull * dim);
+  if (e == cudaSuccess && dual) e = cudaMalloc(&v.locks, nb * 4);
+  if (e == cudaSuccess && hbm_rows < capacity) {
+    e = cudaHostAlloc(reinterpret_cast<void**>(&t->host_slab), (capacity - hbm_rows) * 4ull * dim,
+                      cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess)
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&v.values_host), t->host_slab, 0);
+  }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&t->aux, cudaStreamNonBlocking);
+  if (e == cudaSuccess) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    e = cudaMemPoolCreate(&t->pool, &props);
+    if (e == cudaSuccess) {
+      uint64_t keep = ~0ull;  // keep scratch cached between calls
+      e = cudaMemPoolSetAttribute(t->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+  }
+  if (e == cudaSuccess) e = hkv::launch_clear_table(v, t->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(t->aux);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    release(t);
+    return from_cuda(e);
+  }
+  *out = t;
+  return HKV_OK;
+}
+
+hkv_status hkv_destroy(hkv_table* table) {
+  if (!table) return HKV_OK;
+  {
+    std::lock_guard<std::mutex> lk(table->mu);
+  }
+  release(table);
+  return HKV_OK;
+}
+
+hkv_status hkv_find(hkv_table* t, uint64_t n, const uint64_t* keys, float* values_out,
+                    uint8_t* found_out, uint64_t* scores_out, void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !values_out || !found_out)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kReader, stream, [&](cudaStream_t s) {
+    return from_cuda(hkv::launch_find(t->v, n, keys, values_out, found_out, scores_out, s));
+  });
+}
+
+namespace {
+
+// Call-owned scratch from the table's stream-ordered memory pool; freed on
+// the same stream after the kernels, so concurrent calls never share it.
+hkv_status scratch_call(hkv_table* t, cudaStream_t s, uint64_t n, bool groups, void** mem) {
+  const size_t bytes = hkv::upsert_scratch_bytes(n, t->v.num_buckets, groups);
+  cudaError_t e = cudaMallocFromPoolAsync(mem, bytes, t->pool, s);
+  return from_cuda(e);
+}
+
+}  // namespace
+
+hkv_status hkv_insert_or_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
+                                const uint64_t* scores, void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !values)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
+    const uint64_t step_score = t->step;
+    if (!scores) ++t->step;
+    if (n == 0) return HKV_OK;
+    const bool groups = !t->v.dual;
+    void* mem = nullptr;
+    hkv_status st = scratch_call(t, s, n, groups, &mem);
+    if (st != HKV_OK) return st;
+    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, groups);
+    cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, groups, s);
+    if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
+    cudaError_t f = cudaFreeAsync(mem, s);
+    return from_cuda(e != cudaSuccess ? e : f);
+  });
+}
+
+hkv_status hkv_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
+                      const uint64_t* scores, void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !values)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kUpdater, stream, [&](cudaStream_t s) -> hkv_status {
+    if (n == 0) return HKV_OK;
+    void* mem = nullptr;
+    hkv_status st = scratch_call(t, s, n, false, &mem);
+    if (st != HKV_OK) return st;
+    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, false);
+    cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, false, s);
+    if (e == cudaSuccess) e = hkv::launch_assign(t->v, sc, n, keys, values, scores, s);
+    cudaError_t f = cudaFreeAsync(mem, s);
+    return from_cuda(e != cudaSuccess ? e : f);
+  });
+}
+
+hkv_status hkv_erase(hkv_table* t, uint64_t n, const uint64_t* keys, void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && !keys) return HKV_ERR_INVALID;
+  return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) {
+    return from_cuda(hkv::launch_erase(t->v, n, keys, s));
+  });
+}
+
+hkv_status hkv_size(hkv_table* t, uint64_t* size_host, void* stream) {
+  if (!t || !size_host) return HKV_ERR_INVALID;
+  unsigned long long v = 0;
+  hkv_status st = run_call(t, Role::kReader, stream, [&](cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(&v, &t->v.stats->size, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return from_cuda(e);
+  });
+  if (st == HKV_OK) *size_host = v;
+  return st;
+}
+
+hkv_status hkv_export(hkv_table* t, uint64_t slot_begin, uint64_t slot_end, uint64_t min_score,
+                      uint64_t* keys_out, float* values_out, uint64_t* scores_out,
+                      uint64_t* count_out, void* stream) {
+  if (!t || !keys_out || !count_out) return HKV_ERR_INVALID;
+  if (slot_end > t->capacity) slot_end = t->capacity;
+  if (slot_begin > slot_end) slot_begin = slot_end;
+  return run_call(t, Role::kReader, stream, [&](cudaStream_t s) {
+    return from_cuda(hkv::launch_export(t->v, slot_begin, slot_end, min_score, keys_out, values_out,
+                                        scores_out, count_out, s));
+  });
+}
+
+static hkv_status read_stats(hkv_table* t, hkv::DeviceStats* out) {
+  std::lock_guard<std::mutex> lk(t->mu);
+  DeviceGuard g(t->device);
+  cudaError_t e = t->roles.wait_all();
+  if (e == cudaSuccess) e = cudaMemcpy(out, t->v.stats, sizeof(*out), cudaMemcpyDeviceToHost);
+  return from_cuda(e);
+}
+
+hkv_status hkv_get_error_counts(hkv_table* t, uint64_t* reserved_keys_host, uint64_t* timeouts_host) {
+  if (!t || !reserved_keys_host || !timeouts_host) return HKV_ERR_INVALID;
+  hkv::DeviceStats s{};
+  hkv_status st = read_stats(t, &s);
+  if (st != HKV_OK) return st;
+  *reserved_keys_host = s.reserved;
+  *timeouts_host = s.timeouts;
+  if (s.timeouts) return HKV_ERR_TIMEOUT;
+  if (s.reserved) return HKV_ERR_RESERVED_KEY;
+  return HKV_OK;
+}
+
+hkv_status hkv_get_op_counts(hkv_table* t, hkv_op_counts* out) {
+  if (!t || !out) return HKV_ERR_INVALID;
+  hkv::DeviceStats s{};
+  hkv_status st = read_stats(t, &s);
+  if (st != HKV_OK) return st;
+  out->updated = s.updated;
+  out->admitted = s.admitted;
+  out->evicted = s.evicted;
+  out->rejected = s.rejected;
+  out->erased = s.erased;
+  return HKV_OK;
+}
+
+hkv_status hkv_reset_op_counts(hkv_table* t) {
+  if (!t) return HKV_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(t->mu);
+  DeviceGuard g(t->device);
+  cudaError_t e = t->roles.wait_all();
+  // updated .. erased are contiguous in DeviceStats
+  if (e == cudaSuccess)
+    e = cudaMemset(&t->v.stats->updated, 0,
+                   offsetof(hkv::DeviceStats, size) - offsetof(hkv::DeviceStats, updated));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return from_cuda(e);
+}
+
+hkv_status hkv_get_info(hkv_table* t, hkv_info* out) {
+  if (!t || !out) return HKV_ERR_INVALID;
+  out->capacity = t->capacity;
+  out->num_buckets = t->v.num_buckets;
+  out->hbm_value_rows = t->v.hbm_rows;
+  out->dim = t->v.dim;
+  out->mode = t->mode;
+  out->device = t->device;
+  return HKV_OK;
+}
+
+const char* hkv_status_string(hkv_status s) {
+  switch (s) {
+    case HKV_OK: return "ok";
+    case HKV_ERR_INVALID: return "invalid argument";
+    case HKV_ERR_OOM: return "out of memory";
+    case HKV_ERR_CUDA: return "CUDA error";
+    case HKV_ERR_RESERVED_KEY: return "reserved keys were skipped";
+    case HKV_ERR_TIMEOUT: return "keys abandoned after a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+/*
+ * hkv.h -- C ABI of a cache-semantic GPU key-value hash table (GB300, sm_103a).
+ *
+ * The operations follow "HierarchicalKV: A GPU Hash Table with Cache
+ * Semantics for Continuous Online Embedding Storage" (arXiv 2603.17168v1),
+ * cited below as HKV.  Keys are uint64, scores uint64, values float32 rows of
+ * `dim` elements.  A table of capacity C has B = C / 128 buckets of 128 slots
+ * (HKV §3.2).  Every key lives in one bucket b1 = H(k) mod B (single mode) or
+ * in one of two buckets b1, b2 (dual mode, HKV §3.4), where H is the 64-bit
+ * MurmurHash3 finalizer and b2 = H(k ^ 0x9E3779B97F4A7C15) mod B, moved to
+ * (b1 + 1) mod B when it equals b1.
+ *
+ * Reserved keys: 0xFFFFFFFFFFFFFFF0 .. 0xFFFFFFFFFFFFFFFF are sentinels of
+ * the table.  An input key in that range is skipped by every call (find
+ * reports it not found) and counted; see hkv_get_error_counts.
+ *
+ * Ranks: an entry's rank is the pair (score, key) compared lexicographically
+ * as unsigned integers.  Admission and victim choice use the rank, so equal
+ * scores are decided by key.
+ *
+ * Batches: duplicate keys inside one insert_or_assign or assign batch
+ * collapse to their last occurrence.  Inside one insert_or_assign call the
+ * keys already resident are updated first, then the absent keys are placed;
+ * in single mode the result is therefore a pure function of the table and the
+ * batch (bucket b ends up with the 128 highest-ranked of its residents and of
+ * the absent keys hashed to it).  In dual mode the placement of absent keys
+ * depends on the order the GPU processes them.
+ *
+ * Memory: all pointer arguments except the `*_host` ones are device pointers
+ * (or pointers the device can dereference: mapped or managed host memory).
+ * The caller owns them; they must stay valid until the stream reaches the
+ * call.  The table owns its storage.  Row-major value buffers hold n * dim
+ * float32; a 16-byte aligned base and dim % 4 == 0 select the vector path.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Every batched call is asynchronous: it validates its arguments,
+ * enqueues kernels and returns.  Argument errors are returned at once and
+ * enqueue nothing.
+ *
+ * Roles (HKV §3.5, Table 4): find, size and export are readers; assign is an
+ * updater; insert_or_assign and erase are inserters.  Calls of conflicting
+ * roles issued on different streams are ordered by CUDA events in host issue
+ * order: readers overlap readers, updaters overlap updaters, an inserter
+ * overlaps nothing.  Calls on one table may come from several host threads.
+ */
+#ifndef HKV_H_
+#define HKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hkv_table hkv_table; /* opaque, owned by the library */
+typedef int hkv_status;
+
+enum {
+  HKV_MODE_SINGLE = 0, /* one candidate bucket per key (HKV §3.2) */
+  HKV_MODE_DUAL = 1,   /* two candidate buckets, score-based choice (HKV §3.4) */
+  HKV_MODE_TIERED = 2  /* flag: values above the HBM budget live in mapped host memory (HKV §3.6) */
+};
+
+enum {
+  HKV_OK = 0,
+  HKV_ERR_INVALID = -1,      /* bad argument; nothing was enqueued */
+  HKV_ERR_OOM = -2,          /* device or pinned host allocation failed */
+  HKV_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+  HKV_ERR_RESERVED_KEY = -4, /* hkv_get_error_counts: reserved keys were skipped */
+  HKV_ERR_TIMEOUT = -5       /* hkv_get_error_counts: keys were abandoned after a bounded wait */
+};
+
+#define HKV_SLOTS_PER_BUCKET 128
+#define HKV_RESERVED_KEY_LO 0xFFFFFFFFFFFFFFF0ull
+#define HKV_MAX_BATCH 0x7FFFFFFFull /* largest n accepted by a batched call */
+
+/* Create a table.  HKV §3.1-§3.2 (bucketed layout), §3.6/§4.2 (tiered).
+ *  capacity        slots; a positive multiple of 128 (B = capacity / 128;
+ *                  B >= 2 in dual mode).
+ *  dim             float32 elements per value row, >= 1.
+ *  mode            HKV_MODE_SINGLE or HKV_MODE_DUAL, optionally | HKV_MODE_TIERED.
+ *  value_hbm_bytes with TIERED: HBM budget for value rows.  Rows of whole
+ *                  buckets 0 .. R-1 (R = floor(budget / (128 * 4 * dim)) * 128)
+ *                  live in HBM, the rest in mapped pinned host memory.
+ *                  Ignored without TIERED (all rows in HBM).
+ *  device          CUDA device ordinal the table lives on.
+ *  out             receives the table handle.
+ * Keys, digests and scores always live in HBM.  The table starts empty.
+ * Synchronous.  Errors: INVALID, OOM, CUDA (nothing is leaked). */
+hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t value_hbm_bytes,
+                      int device, hkv_table** out);
+
+/* Wait for all work on the table and free it.  NULL is a no-op. */
+hkv_status hkv_destroy(hkv_table* table);
+
+/* Reader.  HKV Algorithm 1 (digest-accelerated find; two buckets in dual
+ * mode).  For each i < n: if keys[i] is resident, found_out[i] = 1,
+ * values_out[i*dim .. +dim) = its value row and, when scores_out != NULL,
+ * scores_out[i] = its score; otherwise found_out[i] = 0 and the value and
+ * score outputs of row i are left untouched.  The table is not modified. */
+hkv_status hkv_find(hkv_table* table, uint64_t n, const uint64_t* keys, float* values_out,
+                    uint8_t* found_out, uint64_t* scores_out, void* stream);
+
+/* Inserter.  HKV Algorithm 2 (single mode) / Algorithm 3 (dual mode):
+ * upsert with bucket-local admission and eviction.  A resident key gets the
+ * new value and score unconditionally.  An absent key takes a free slot of
+ * its bucket (dual mode: the less occupied candidate, ties to b1); when the
+ * bucket is full (dual: both full) it replaces the lowest-ranked entry of the
+ * bucket (dual: of the candidate whose lowest rank is lower) if it ranks
+ * higher than that entry, else it is rejected.
+ *  scores  per-key scores, or NULL: every key of the call gets the table's
+ *          step counter, which starts at 1 and grows by 1 per NULL-score call.
+ * Outcome totals accumulate in hkv_get_op_counts. */
+hkv_status hkv_insert_or_assign(hkv_table* table, uint64_t n, const uint64_t* keys,
+                                const float* values, const uint64_t* scores, void* stream);
+
+/* Updater.  HKV §3.5: overwrites the value (and the score when scores !=
+ * NULL) of resident keys in place; absent keys are ignored; nothing is
+ * inserted, evicted or moved. */
+hkv_status hkv_assign(hkv_table* table, uint64_t n, const uint64_t* keys, const float* values,
+                      const uint64_t* scores, void* stream);
+
+/* Inserter.  HKV §3.5: removes each resident key; its slot becomes free. */
+hkv_status hkv_erase(hkv_table* table, uint64_t n, const uint64_t* keys, void* stream);
+
+/* Reader.  HKV §3.5 (size): number of resident entries, written to the host
+ * variable *size_host.  Synchronises with `stream`. */
+hkv_status hkv_size(hkv_table* table, uint64_t* size_host, void* stream);
+
+/* Reader.  HKV §4.1 export_batch_if with the predicate score >= min_score
+ * (the score-threshold dump of the DynamicEmb API page).  Scans slots
+ * [slot_begin, slot_end) (slot = bucket * 128 + position, end clamped to the
+ * capacity) and writes each matching entry to keys_out / values_out /
+ * scores_out (values_out and scores_out may be NULL) at consecutive
+ * positions in unspecified order.  *count_out (device) receives the number
+ * written; outputs must have room for slot_end - slot_begin entries. */
+hkv_status hkv_export(hkv_table* table, uint64_t slot_begin, uint64_t slot_end, uint64_t min_score,
+                      uint64_t* keys_out, float* values_out, uint64_t* scores_out,
+                      uint64_t* count_out, void* stream);
+
+/* Cumulative counts since creation, read synchronously (waits for the
+ * table's outstanding work).  reserved_keys: input keys skipped because they
+ * were reserved sentinels.  timeouts: keys abandoned after a bounded wait on
+ * a bucket lock (dual mode); nonzero means those keys were not applied.
+ * Returns HKV_ERR_TIMEOUT when timeouts > 0, else HKV_ERR_RESERVED_KEY when
+ * reserved_keys > 0, else HKV_OK; the counts are written in every case. */
+hkv_status hkv_get_error_counts(hkv_table* table, uint64_t* reserved_keys_host,
+                                uint64_t* timeouts_host);
+
+/* Cumulative outcome totals of insert_or_assign / assign / erase since
+ * creation (or the last reset), read synchronously.  For insert_or_assign:
+ * updated = resident keys overwritten; admitted = absent keys resident after
+ * their call; rejected = absent keys not resident after their call; evicted =
+ * keys resident before a call that it displaced.  assign adds to updated,
+ * erase to erased. */
+typedef struct hkv_op_counts {
+  uint64_t updated, admitted, evicted, rejected, erased;
+} hkv_op_counts;
+hkv_status hkv_get_op_counts(hkv_table* table, hkv_op_counts* out_host);
+hkv_status hkv_reset_op_counts(hkv_table* table);
+
+/* Static facts about a table. */
+typedef struct hkv_info {
+  uint64_t capacity, num_buckets, hbm_value_rows;
+  uint32_t dim, mode;
+  int device;
+} hkv_info;
+hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
+
+/* Human-readable name of a status code (static storage). */
+const char* hkv_status_string(hkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HKV_H_ */
