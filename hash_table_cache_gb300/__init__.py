@@ -42,8 +42,9 @@ RESERVED_KEY_LO = 0xFFFFFFFFFFFFFFF0
 EXPORTS = (
     "hkv_create", "hkv_destroy", "hkv_find", "hkv_insert_or_assign", "hkv_assign", "hkv_erase",
     "hkv_size", "hkv_export", "hkv_get_error_counts", "hkv_get_op_counts",
-    "hkv_reset_op_counts", "hkv_get_info", "hkv_status_string",
+    "hkv_reset_op_counts", "hkv_get_info", "hkv_status_string", "hkv_insert_or_assign_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class HKVError(RuntimeError):
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
         "hkv_destroy": [vp],
         "hkv_find": [vp, u64, vp, vp, vp, vp, vp],
         "hkv_insert_or_assign": [vp, u64, vp, vp, vp, vp],
+        "hkv_insert_or_assign_noalloc": [vp, u64, vp, vp, vp, vp],
         "hkv_assign": [vp, u64, vp, vp, vp, vp],
         "hkv_erase": [vp, u64, vp, vp],
         "hkv_size": [vp, ctypes.POINTER(u64), vp],
@@ -146,6 +148,14 @@ def hkv_find(table, n, keys, values_out, found_out, scores_out=None, stream=None
 
 def hkv_insert_or_assign(table, n, keys, values, scores=None, stream=None):
     return load().hkv_insert_or_assign(table, int(n), _p(keys), _p(values), _p(scores), _s(stream))
+
+
+def hkv_insert_or_assign_noalloc(table, n, keys, values, scores=None, stream=None):
+    """insert_or_assign without any allocation by the library: its working
+    memory is a fixed array inside libhkv.so (see include/hkv.h for the size
+    limit, the sharing rule and the first-call set-up)."""
+    return load().hkv_insert_or_assign_noalloc(table, int(n), _p(keys), _p(values), _p(scores),
+                                               _s(stream))
 
 
 def hkv_assign(table, n, keys, values, scores=None, stream=None):

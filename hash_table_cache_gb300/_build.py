@@ -12,7 +12,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["table.cu", "find.cu", "upsert.cu", "export.cu"]
+SOURCES = ["table.cu", "find.cu", "upsert.cu", "export.cu", "no_alloc.cu"]
 
 
 def _nvcc():

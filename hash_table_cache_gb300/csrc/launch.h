@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "hkv.h"
 
 namespace hkv {
 
@@ -50,5 +51,12 @@ cudaError_t launch_clear_table(const TableView& t, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Runs insert_or_assign with caller-provided working memory (used by
+// hkv_insert_or_assign_noalloc); get_scratch(device, &ptr) yields it.
+struct NoAllocAccess {
+  static int run(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
+                 const uint64_t* scores, void* stream, cudaError_t (*get_scratch)(int, void**));
+};
 
 }  // namespace hkv

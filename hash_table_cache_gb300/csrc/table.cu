@@ -178,6 +178,35 @@ hkv_status run_call(hkv_table* t, Role r, void* stream, F&& body) {
 
 }  // namespace
 
+namespace hkv {
+
+int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
+                       const uint64_t* scores, void* stream,
+                       cudaError_t (*get_scratch)(int, void**)) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !values)) return HKV_ERR_INVALID;
+  const bool groups = !t->v.dual;
+  if (upsert_scratch_bytes(n, t->v.num_buckets, groups) > HKV_NOALLOC_SCRATCH_BYTES)
+    return HKV_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(t->mu);
+  DeviceGuard g(t->device);
+  void* mem = nullptr;
+  cudaError_t e = get_scratch(t->device, &mem);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = t->roles.before(Role::kInserter, s);  // waits only: records no event
+  if (e != cudaSuccess) return from_cuda(e);
+  const uint64_t step_score = t->step;
+  if (!scores) ++t->step;
+  if (n == 0) return HKV_OK;
+  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, groups);
+  e = clear_upsert_scratch(sc, t->v.num_buckets, groups, s);
+  if (e == cudaSuccess) e = launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
+  return from_cuda(e);
+}
+
+}  // namespace hkv
+
 extern "C" {
 
 hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t value_hbm_bytes,

@@ -167,6 +167,38 @@ typedef struct hkv_info {
 } hkv_info;
 hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
 
+/* insert_or_assign for callers that cannot let the library allocate.
+ *
+ * The paper has no counterpart: this is a deployment variant of
+ * hkv_insert_or_assign with the same arguments and the same results.  That
+ * call takes its per-call working memory from a stream-ordered pool; this
+ * one uses a fixed array of HKV_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, for callers whose device memory is already handed out (e.g. to a
+ * framework's caching allocator), who keep a fixed memory budget, or whose
+ * serving loop must never enter cudaMalloc/cudaFree (which can synchronise
+ * the device).  It calls no allocation routine.
+ *  - Limit: the batch's working memory must fit the array, i.e.
+ *      a(8M) + a(4M) + 256 + (single mode only) 3 a(4n) + 2 a(4B) bytes,
+ *    with M the smallest power of two >= max(64, 2n), B the bucket count and
+ *    a(x) = x rounded up to a multiple of 256.  Larger batches return
+ *    HKV_ERR_INVALID and enqueue nothing (split them, or use
+ *    hkv_insert_or_assign).  Single mode with 32,768 buckets takes up to
+ *    2^19 keys per call.
+ *  - Sharing: every call on every table of a device uses the same array and
+ *    clears it before use.  Calls whose kernels overlap on the GPU (on
+ *    different streams, from any table) race on it and corrupt each other's
+ *    results: keep such calls on one stream, or order them with events.
+ *  - Ordering: the call waits for earlier conflicting calls on this table
+ *    like hkv_insert_or_assign, but records no event of its own; later calls
+ *    on other streams do not wait for it.  Issue them on the same stream or
+ *    order them yourself.
+ *  - Set-up: the first call on a device (made with any table of that device)
+ *    looks up the array's device address with cudaGetSymbolAddress and keeps
+ *    it; make that first call before any stream capture. */
+#define HKV_NOALLOC_SCRATCH_BYTES (32ull << 20)
+hkv_status hkv_insert_or_assign_noalloc(hkv_table* table, uint64_t n, const uint64_t* keys,
+                                        const float* values, const uint64_t* scores, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* hkv_status_string(hkv_status status);
 
