@@ -227,8 +227,12 @@ def run_gpu(args):
     res = res.cpu().numpy().view(np.uint64)
     nsteps = args.warmup + args.steps
     up_k, up_v, fq = [], [], []
+    prev = res
     for s in range(nsteps):
-        q, _ = wl.hit_mix(100 + s + seed_base, res, 200 + seed_base, BATCH, HIT, fresh_start=s * BATCH)
+        # upsert: 80% drawn from keys resident before this step (the previous
+        # step's upsert keys, all resident after it), 20% fresh
+        q, _ = wl.hit_mix(100 + s + seed_base, prev, 200 + seed_base, BATCH, HIT, fresh_start=s * BATCH)
+        prev = q
         qd = dk(q)
         up_k.append(qd)
         up_v.append(wl.key_values_torch(qd, DIM, salt=3 + s))

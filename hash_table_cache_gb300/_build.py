@@ -26,10 +26,13 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB) -> str:
+    """Compile every source and link `out` (default: the in-tree libhkv.so).
+    `extra_flags` are passed to nvcc (e.g. -D tuning macros)."""
+    if not force and out == LIB and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if out == LIB else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
              "-I", INCLUDE, "-I", CSRC, *extra_flags]
@@ -37,7 +40,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -49,13 +52,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if verbose:
         for _, err in results:
             print(err)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -4,8 +4,9 @@
 // Layout in HBM (HierarchicalKV §3.2 Figure 4, §3.6, §4.2): structure of
 // arrays over B buckets of 128 slots; slot j of bucket b is row r = b*128 + j.
 //   digests[B*128]  uint8   one 128-byte line per bucket, 0 = free slot
-//   keys[B*128]     uint64  EMPTY_KEY marks a free slot
-//   scores[B*128]   uint64
+//   slots[B*128]    {uint64 key, uint64 score}; EMPTY_KEY marks a free slot
+//                   (key and score share one 32-byte sector, so a find hit
+//                   reads its score with the key confirm)
 //   values          float32 rows of `dim`; rows < hbm_rows in HBM, the rest in
 //                   mapped pinned host memory (tiered mode)
 // No per-entry pointer is stored: a value row is found from (bucket, slot).
@@ -38,8 +39,7 @@ struct DeviceStats {
 // Everything a kernel needs to address the table; passed by value.
 struct TableView {
   uint8_t* digests;
-  uint64_t* keys;
-  uint64_t* scores;
+  uint64_t* slots;        // 2 words per slot: key, score
   float* values_hbm;
   float* values_host;     // device pointer of the mapped host slab, or null
   uint64_t hbm_rows;      // rows below this index live in values_hbm
@@ -83,6 +83,13 @@ __host__ __device__ __forceinline__ uint32_t digest_of_hash(uint64_t h) {
 }
 
 __device__ __forceinline__ bool is_reserved(uint64_t k) { return k >= kReservedLo; }
+
+__device__ __forceinline__ uint64_t* key_at(const TableView& t, uint64_t row) {
+  return t.slots + 2 * row;
+}
+__device__ __forceinline__ uint64_t* score_at(const TableView& t, uint64_t row) {
+  return t.slots + 2 * row + 1;
+}
 
 __device__ __forceinline__ float* row_ptr(const TableView& t, uint64_t row) {
   return row < t.hbm_rows ? t.values_hbm + row * t.dim
@@ -140,6 +147,23 @@ __device__ __forceinline__ uint32_t byte_eq_mask4(uint32_t w, uint32_t pat) {
   return ((z >> 7) & 1u) | ((z >> 14) & 2u) | ((z >> 21) & 4u) | ((z >> 28) & 8u);
 }
 
+// Zero-byte flags of x: bit 8i+7 is set for every zero byte i of x, and may
+// also be set for a byte directly above a zero byte (borrow).  A word with no
+// zero byte gives 0.  Used on (digest word ^ pattern): a flagged byte is a
+// candidate slot whose key is then compared, so an extra flag costs one key
+// comparison and never a wrong result.
+__device__ __forceinline__ uint32_t zero_byte_flags(uint32_t x) {
+  return (x - 0x01010101u) & ~x & 0x80808080u;
+}
+
+// Candidate mask of the four bytes of w against the replicated digest `pat`:
+// bit i set when byte i may equal the digest (every equal byte is set; see
+// zero_byte_flags for the rare extra).  The multiply gathers the flag bits
+// 7, 15, 23, 31 into bits 28..31 without carries.
+__device__ __forceinline__ uint32_t byte_match4(uint32_t w, uint32_t pat) {
+  return (zero_byte_flags(w ^ pat) * 0x00204081u) >> 28;
+}
+
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
 // Warp-aggregated atomic add of a per-lane contribution (any lane set).
@@ -166,6 +190,31 @@ __device__ __forceinline__ void tile_copy_row(float* dst, const float* src, uint
   }
 }
 
+// Copy R value rows with the 8 lanes of a tile, all R loads of a chunk in
+// flight before the stores (rows with ok[r] == false are skipped).
+template <int R>
+__device__ __forceinline__ void tile_copy_rows(float* const (&dst)[R], const float* const (&src)[R],
+                                               const bool (&ok)[R], uint32_t dim, unsigned sub,
+                                               bool vec) {
+  if (vec) {
+    const uint32_t chunks = dim >> 2;
+    for (uint32_t c = sub; c < chunks; c += 8) {
+      uint4 v[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (ok[r]) v[r] = ld_stream_v4(src[r] + 4 * c);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (ok[r]) st_stream_v4(dst[r] + 4 * c, v[r]);
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (ok[r])
+        for (uint32_t c = sub; c < dim; c += 8) dst[r][c] = src[r][c];
+  }
+}
+
 // Probe bucket b for `key` with the 8 lanes of a tile (HKV Algorithm 1):
 // lane `sub` loads 16 bytes of the 128-byte digest line, byte-compares them
 // with the key's digest (`pat` = digest * 0x01010101) and confirms each match
@@ -179,14 +228,14 @@ __device__ __forceinline__ int tile_probe(const TableView& t, uint64_t b, uint64
   uint4 dg;
   if (kNC) dg = ld_nc_v4(dp);
   else dg = ld_cg_v4(dp);
-  uint32_t m = byte_eq_mask4(dg.x, pat) | (byte_eq_mask4(dg.y, pat) << 4) |
-               (byte_eq_mask4(dg.z, pat) << 8) | (byte_eq_mask4(dg.w, pat) << 12);
+  uint32_t m = byte_match4(dg.x, pat) | (byte_match4(dg.y, pat) << 4) |
+               (byte_match4(dg.z, pat) << 8) | (byte_match4(dg.w, pat) << 12);
   int hit = -1;
-  const uint64_t* kb = t.keys + b * kSlots + sub * 16;
+  const uint64_t* kb = t.slots + 2 * (b * kSlots + sub * 16);
   while (m) {
     const int bit = __ffs(m) - 1;
     m &= m - 1;
-    const uint64_t k = kNC ? ld_nc_u64(kb + bit) : ld_cg_u64(kb + bit);
+    const uint64_t k = kNC ? ld_nc_u64(kb + 2 * bit) : ld_cg_u64(kb + 2 * bit);
     if (k == key) {
       hit = static_cast<int>(sub * 16 + bit);
       break;

@@ -19,14 +19,15 @@ __global__ void __launch_bounds__(kThreads) export_kernel(TableView t, uint64_t 
   const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
   for (uint64_t row = slot_begin + ((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3);
        row < slot_end; row += tiles) {
-    const uint64_t k = t.keys[row];
-    const bool take = k < kReservedLo && t.scores[row] >= min_score;
+    const ulonglong2 ks = *reinterpret_cast<const ulonglong2*>(key_at(t, row));
+    const uint64_t k = ks.x;
+    const bool take = k < kReservedLo && ks.y >= min_score;
     if (!take) continue;  // tile-uniform
     unsigned long long pos = 0;
     if (sub == 0) {
       pos = atomicAdd(count, 1ull);
       keys_out[pos] = k;
-      if (scores_out) scores_out[pos] = t.scores[row];
+      if (scores_out) scores_out[pos] = ks.y;
     }
     pos = __shfl_sync(tmask, pos, lane & 24u);
     if (values_out)
@@ -53,9 +54,9 @@ cudaError_t launch_export(const TableView& t, uint64_t slot_begin, uint64_t slot
 
 cudaError_t launch_clear_table(const TableView& t, cudaStream_t st) {
   const uint64_t slots = t.num_buckets * kSlots;
-  cudaError_t e = cudaMemsetAsync(t.keys, 0xFF, slots * 8, st);
+  // every slot free: key = EMPTY (all ones); a free slot's score is never read
+  cudaError_t e = cudaMemsetAsync(t.slots, 0xFF, slots * 16, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(t.digests, 0, slots, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(t.scores, 0, slots * 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(t.stats, 0, sizeof(DeviceStats), st);
   if (e == cudaSuccess && t.locks) e = cudaMemsetAsync(t.locks, 0, t.num_buckets * 4, st);
   return e;

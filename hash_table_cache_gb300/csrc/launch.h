@@ -11,23 +11,26 @@ namespace hkv {
 
 // Scratch of one insert_or_assign / assign call (device memory, call-owned).
 struct UpsertScratch {
-  uint64_t* map_keys;   // dedup map, map_size entries, EMPTY-initialised
-  uint32_t* map_idx;    // last batch index + 1 per map entry, 0-initialised
-  uint32_t map_size;    // power of two
-  uint32_t* bkt;        // per key: its bucket if it is a last occurrence, else kNone
-  uint32_t* rnk;        // per key: position inside its bucket group
-  uint32_t* cnt;        // per bucket: group size (0-initialised)
-  uint32_t* off;        // per bucket: group start in `group`
-  uint32_t* group;      // batch indices grouped by bucket
-  uint32_t* cursor;     // bump allocator for group starts / miss list length (0-initialised)
+  uint64_t* map_keys;   // map_size entries, EMPTY-initialised: the single-mode
+                        // stage, or the dedup map of dual mode and assign
+  uint32_t* map_idx;    // last batch index + 1 per entry, 0-initialised
+  uint32_t map_size;    // power of two, >= 2n
+  int32_t area_shift;   // single mode, power-of-two bucket count B: log2(S/B)
+                        // (negative: B > S); kNoShift otherwise
+  uint32_t* cursor;     // small counters (0-initialised)
+  uint8_t* mark;        // single mode: one byte per table bucket, 1 = holds batch keys
+  uint32_t* group;      // dual mode: indices of the batch's absent keys
 };
 
-// Bytes of scratch an insert_or_assign / assign of n keys needs, and the
-// carving of one allocation into the UpsertScratch arrays.
-size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, bool need_groups);
-UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, bool need_groups);
+// What a call needs scratch for.
+enum class ScratchKind { kSingleUpsert, kDualUpsert, kAssign };
+
+// Bytes of scratch a call of n keys needs, and the carving of one allocation
+// into the UpsertScratch arrays.
+size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind);
+UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind);
 // Enqueue the clears the scratch needs before use.
-cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, bool need_groups,
+cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st);
 
 cudaError_t launch_find(const TableView& t, uint64_t n, const uint64_t* keys, float* values_out,

@@ -150,8 +150,7 @@ void release(hkv_table* t) {
   if (t->aux) cudaStreamDestroy(t->aux);
   if (t->pool) cudaMemPoolDestroy(t->pool);
   cudaFree(t->v.digests);
-  cudaFree(t->v.keys);
-  cudaFree(t->v.scores);
+  cudaFree(t->v.slots);
   cudaFree(t->v.values_hbm);
   cudaFree(t->v.locks);
   cudaFree(t->v.stats);
@@ -185,8 +184,8 @@ int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const flo
                        cudaError_t (*get_scratch)(int, void**)) {
   if (!batch_ok(t, n)) return HKV_ERR_INVALID;
   if (n && (!keys || !values)) return HKV_ERR_INVALID;
-  const bool groups = !t->v.dual;
-  if (upsert_scratch_bytes(n, t->v.num_buckets, groups) > HKV_NOALLOC_SCRATCH_BYTES)
+  const ScratchKind kind = t->v.dual ? ScratchKind::kDualUpsert : ScratchKind::kSingleUpsert;
+  if (upsert_scratch_bytes(n, t->v.num_buckets, kind) > HKV_NOALLOC_SCRATCH_BYTES)
     return HKV_ERR_INVALID;
   std::lock_guard<std::mutex> lk(t->mu);
   DeviceGuard g(t->device);
@@ -199,8 +198,8 @@ int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const flo
   const uint64_t step_score = t->step;
   if (!scores) ++t->step;
   if (n == 0) return HKV_OK;
-  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, groups);
-  e = clear_upsert_scratch(sc, t->v.num_buckets, groups, s);
+  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, kind);
+  e = clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
   if (e == cudaSuccess) e = launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
   return from_cuda(e);
 }
@@ -244,8 +243,7 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
   v.hbm_rows = hbm_rows;
 
   cudaError_t e = cudaMalloc(&v.digests, capacity);
-  if (e == cudaSuccess) e = cudaMalloc(&v.keys, capacity * 8);
-  if (e == cudaSuccess) e = cudaMalloc(&v.scores, capacity * 8);
+  if (e == cudaSuccess) e = cudaMalloc(&v.slots, capacity * 16);
   if (e == cudaSuccess) e = cudaMalloc(&v.stats, sizeof(hkv::DeviceStats));
   if (e == cudaSuccess && hbm_rows) e = cudaMalloc(&v.values_hbm, hbm_rows * 4ull * dim);
   if (e == cudaSuccess && dual) e = cudaMalloc(&v.locks, nb * 4);
@@ -300,8 +298,9 @@ namespace {
 
 // Call-owned scratch from the table's stream-ordered memory pool; freed on
 // the same stream after the kernels, so concurrent calls never share it.
-hkv_status scratch_call(hkv_table* t, cudaStream_t s, uint64_t n, bool groups, void** mem) {
-  const size_t bytes = hkv::upsert_scratch_bytes(n, t->v.num_buckets, groups);
+hkv_status scratch_call(hkv_table* t, cudaStream_t s, uint64_t n, hkv::ScratchKind kind,
+                        void** mem) {
+  const size_t bytes = hkv::upsert_scratch_bytes(n, t->v.num_buckets, kind);
   cudaError_t e = cudaMallocFromPoolAsync(mem, bytes, t->pool, s);
   return from_cuda(e);
 }
@@ -316,12 +315,13 @@ hkv_status hkv_insert_or_assign(hkv_table* t, uint64_t n, const uint64_t* keys, 
     const uint64_t step_score = t->step;
     if (!scores) ++t->step;
     if (n == 0) return HKV_OK;
-    const bool groups = !t->v.dual;
+    const hkv::ScratchKind kind =
+        t->v.dual ? hkv::ScratchKind::kDualUpsert : hkv::ScratchKind::kSingleUpsert;
     void* mem = nullptr;
-    hkv_status st = scratch_call(t, s, n, groups, &mem);
+    hkv_status st = scratch_call(t, s, n, kind, &mem);
     if (st != HKV_OK) return st;
-    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, groups);
-    cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, groups, s);
+    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, kind);
+    cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
     if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
     cudaError_t f = cudaFreeAsync(mem, s);
     return from_cuda(e != cudaSuccess ? e : f);
@@ -335,10 +335,12 @@ hkv_status hkv_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const floa
   return run_call(t, Role::kUpdater, stream, [&](cudaStream_t s) -> hkv_status {
     if (n == 0) return HKV_OK;
     void* mem = nullptr;
-    hkv_status st = scratch_call(t, s, n, false, &mem);
+    hkv_status st = scratch_call(t, s, n, hkv::ScratchKind::kAssign, &mem);
     if (st != HKV_OK) return st;
-    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, false);
-    cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, false, s);
+    hkv::UpsertScratch sc =
+        hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, hkv::ScratchKind::kAssign);
+    cudaError_t e =
+        hkv::clear_upsert_scratch(sc, t->v.num_buckets, hkv::ScratchKind::kAssign, s);
     if (e == cudaSuccess) e = hkv::launch_assign(t->v, sc, n, keys, values, scores, s);
     cudaError_t f = cudaFreeAsync(mem, s);
     return from_cuda(e != cudaSuccess ? e : f);

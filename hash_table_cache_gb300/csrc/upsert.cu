@@ -3,33 +3,40 @@
 // dual-bucket upsert), assign and erase (HKV §3.5).
 //
 // Single-bucket insert_or_assign is organised around bucket ownership rather
-// than the paper's per-key CAS protocol:
-//   1. dedup: the keys of the batch go into a scratch hash map that keeps the
-//      largest batch index of each key (duplicates collapse to their last
-//      occurrence);
-//   2. group: each surviving key is counted into its bucket, groups get
-//      disjoint ranges of one index array, and the keys are scattered there;
-//   3. process: one warp owns one bucket.  It loads the bucket's 128 keys
-//      (32 bytes per lane, one coalesced kilobyte), applies the in-place
-//      updates of resident keys, then places the absent keys: a free slot if
-//      there is one, else the 128 scores are loaded once and a warp-shuffle
-//      arg-min over the rank (score, key) decides admission and the victim.
-//      Keys, scores and digests are written back once per bucket and the
-//      value rows of the final occupants are copied by 8-lane tiles.
+// than the paper's per-key CAS protocol.  Two kernels:
+//   1. stage: every key of the batch is entered into a scratch open-addressing
+//      table laid out bucket by bucket: table bucket b owns the positions
+//      [S*b/B, S*(b+1)/B) of the S-entry stage and a key probes linearly from
+//      a hashed position inside its bucket's range.  An entry keeps the largest
+//      batch index of its key, so duplicates collapse to their last
+//      occurrence, and the entries of one table bucket end up in one short
+//      contiguous run of the stage.
+//   2. process: one warp owns one table bucket.  It loads the bucket (128
+//      key/score pairs, two kilobytes, and the digest line) into shared
+//      memory, scans its stage run 32 positions at a time, applies the
+//      in-place updates of resident keys, then places the absent keys: the
+//      free slots in slot order first, then, for each remaining absent key, a
+//      warp arg-min over the rank (score, key) decides admission and the
+//      victim.  Keys, scores and digests are written back once per bucket and
+//      the value rows of the final occupants are copied by 8-lane tiles.
 // With one owner per bucket there is no slot locking and no retry; the result
-// of a bucket depends only on its residents and its group, never on thread
-// scheduling, so it equals the oracle's serial result exactly.
+// of a bucket depends only on its residents and its keys in the batch, never
+// on thread scheduling, so it equals the oracle's serial result exactly.
 //
 // Dual mode couples two buckets per key, so ownership cannot be partitioned:
-// resident keys are updated in place by a tile kernel, then each absent key
-// is placed by one warp holding locks on both candidate buckets (taken in
-// increasing bucket order, bounded spin).
+// the batch is de-duplicated in a scratch map, resident keys are updated in
+// place by a tile kernel, then each absent key is placed by one warp holding
+// locks on both candidate buckets (taken in increasing bucket order, bounded
+// spin).
 #include "launch.h"
 
 namespace hkv {
 namespace {
 
 constexpr int kThreads = 256;
+#ifndef HKV_UPSERT_MIN_BLOCKS
+#define HKV_UPSERT_MIN_BLOCKS 3
+#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 constexpr int kSpinLimit = 1 << 20;
 
@@ -92,50 +99,69 @@ __global__ void __launch_bounds__(kThreads) dedup_insert_kernel(UpsertScratch sc
 }
 
 // ---------------------------------------------------------------------------
-// 2. group: count last occurrences per bucket, assign group ranges, scatter.
+// Single mode, 1. stage.  Bucket b's range of the S-entry stage starts at
+// area_start(b) = S*b/B; `a` = its length (0 when the stage has fewer entries
+// than the table has buckets).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) group_count_kernel(TableView t, UpsertScratch sc,
-                                                               uint64_t n, const uint64_t* keys) {
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += stride) {
-    const uint64_t k = keys[i];
-    uint32_t b = kNone;
-    if (!is_reserved(k) && is_last_occurrence(sc, k, i)) {
-      b = static_cast<uint32_t>(bucket_of_hash(t, hash64(k)));
-      sc.rnk[i] = atomicAdd(sc.cnt + b, 1u);
-    }
-    sc.bkt[i] = b;
-  }
+constexpr int32_t kNoShift = 0x7FFFFFFF;
+
+__device__ __forceinline__ uint64_t area_start(uint64_t b, uint64_t S, uint64_t B, int32_t shift) {
+  if (shift == kNoShift) return (b * S) / B;
+  return shift >= 0 ? (b << shift) : (b >> (-shift));
 }
 
-__global__ void __launch_bounds__(kThreads) group_offsets_kernel(UpsertScratch sc, uint64_t nb) {
-  const unsigned lane = lane_id();
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31u);
-       base < nb; base += stride) {
-    const uint64_t b = base + lane;
-    const uint32_t c = b < nb ? sc.cnt[b] : 0;
-    uint32_t incl = c;
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= static_cast<unsigned>(o)) incl += v;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    uint32_t start = 0;
-    if (lane == 31 && total) start = atomicAdd(sc.cursor, total);
-    start = __shfl_sync(0xFFFFFFFFu, start, 31);
-    if (b < nb && c) sc.off[b] = start + incl - c;
-  }
+__device__ __forceinline__ uint64_t stage_home(uint64_t h, uint64_t lo, uint64_t a) {
+  if (a == 0) return lo;
+  const uint64_t r = h >> 40;
+  return lo + ((a & (a - 1)) == 0 ? (r & (a - 1)) : (r % a));
 }
 
-__global__ void __launch_bounds__(kThreads) group_scatter_kernel(UpsertScratch sc, uint64_t n) {
+constexpr int kStageKeysPerThread = 1;
+
+__global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScratch sc, uint64_t n,
+                                                         const uint64_t* keys) {
+  constexpr int U = kStageKeysPerThread;
+  const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += stride) {
-    const uint32_t b = sc.bkt[i];
-    if (b != kNone) sc.group[sc.off[b] + sc.rnk[i]] = static_cast<uint32_t>(i);
+  unsigned long long reserved = 0;
+  for (uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
+       i0 += stride * U) {
+    uint64_t k[U], pos[U], b[U];
+    bool v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t i = i0 + u * stride;
+      v[u] = i < n;
+      k[u] = v[u] ? keys[i] : kEmptyKey;
+      if (v[u] && is_reserved(k[u])) {
+        ++reserved;
+        v[u] = false;
+      }
+      const uint64_t h = hash64(k[u]);
+      b[u] = bucket_of_hash(t, h);
+      const uint64_t lo = area_start(b[u], S, B, sc.area_shift);
+      pos[u] = stage_home(h, lo, area_start(b[u] + 1, S, B, sc.area_shift) - lo) & mask;
+    }
+    unsigned long long prev[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v[u]) prev[u] = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + pos[u]),
+                                   kEmptyKey, k[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!v[u]) continue;
+      uint64_t p = pos[u];
+      unsigned long long pv = prev[u];
+      // S >= 2n: a free position exists, so the probe ends within S steps
+      for (uint64_t tries = 1; pv != kEmptyKey && pv != k[u] && tries < S; ++tries) {
+        p = (p + 1) & mask;
+        pv = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + p), kEmptyKey, k[u]);
+      }
+      atomicMax(sc.map_idx + p, static_cast<uint32_t>(i0 + u * stride) + 1);
+      sc.mark[b[u]] = 1;  // the bucket holds keys of the batch (plain store)
+    }
   }
+  warp_add(&t.stats->reserved, reserved);
 }
 
 // Rank order (HKV Algorithm 2 arg-min, ties by key): true when (s1,k1) < (s2,k2).
@@ -145,215 +171,366 @@ __device__ __forceinline__ bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2,
 
 // ---------------------------------------------------------------------------
 // 3. process: one warp per bucket (single mode).
-// Lane l holds slots 4l..4l+3: key sk[q], score sc_[q] (valid when the slot
-// is dirty or the scores were loaded), occ[q] = batch index whose value row
-// the slot must receive (kNone = unchanged), bit q of `fresh` = the slot's
-// occupant was admitted by this call.
+// The warp stages its bucket in shared memory: the 128 keys, the digest line,
+// the scores (loaded once the bucket needs an eviction decision, or up front
+// for large groups), and per slot the batch index whose value row the slot
+// must receive (occ; kNone = unchanged) and whether its occupant was admitted
+// by this call (fresh).
 // ---------------------------------------------------------------------------
-struct CopyJob {
-  uint32_t src;  // batch index
-  uint32_t slot; // 0..127
+constexpr int kWin = 4;  // stage chunks (32 positions each) held in registers
+
+struct BucketStage {
+  uint64_t ekey[kWin * 32];  // the bucket's batch entries, compacted
+  uint32_t eidx[kWin * 32];
+  uint64_t key[kSlots];
+  uint64_t score[kSlots];
+  uint32_t occ[kSlots];
+  uint32_t dig[kSlots / 4];
+  uint32_t fresh[kSlots / 32];
+  uint8_t list[kSlots];  // free-slot list, later the dirty-slot list
 };
 
-__global__ void __launch_bounds__(kThreads) upsert_single_kernel(
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Exclusive prefix over lanes of a per-lane count in 0..4 (three bit planes).
+__device__ __forceinline__ uint32_t prefix_small(uint32_t c, uint32_t& total) {
+  const unsigned lt = lanemask_lt();
+  const unsigned p0 = __ballot_sync(0xFFFFFFFFu, c & 1u);
+  const unsigned p1 = __ballot_sync(0xFFFFFFFFu, c & 2u);
+  const unsigned p2 = __ballot_sync(0xFFFFFFFFu, c & 4u);
+  total = __popc(p0) + 2 * __popc(p1) + 4 * __popc(p2);
+  return __popc(p0 & lt) + 2 * __popc(p1 & lt) + 4 * __popc(p2 & lt);
+}
+
+// Warp minimum of a 64-bit value over the lanes with `valid`, by two 32-bit
+// reductions; `sel` receives the lanes that hold it.
+__device__ __forceinline__ uint64_t warp_min_u64(uint64_t v, bool valid, unsigned& sel) {
+  const uint32_t hi = valid ? static_cast<uint32_t>(v >> 32) : 0xFFFFFFFFu;
+  const uint32_t mh = __reduce_min_sync(0xFFFFFFFFu, hi);
+  bool c = valid && hi == mh;
+  const uint32_t lo = c ? static_cast<uint32_t>(v) : 0xFFFFFFFFu;
+  const uint32_t ml = __reduce_min_sync(0xFFFFFFFFu, lo);
+  c = c && static_cast<uint32_t>(v) == ml;
+  sel = __ballot_sync(0xFFFFFFFFu, c);
+  return (static_cast<uint64_t>(mh) << 32) | ml;
+}
+
+__global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
     const uint64_t* scores_in, uint64_t step_score, bool vec) {
-  __shared__ CopyJob jobs_all[kThreads / 32][kSlots];
+  (void)keys_in;  // entry keys come from the stage
+  __shared__ BucketStage stage_all[kThreads / 32];
   const unsigned lane = lane_id();
-  const unsigned warp = threadIdx.x >> 5;
-  CopyJob* jobs = jobs_all[warp];
+  BucketStage& st = stage_all[threadIdx.x >> 5];
   const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   const uint64_t nb = t.num_buckets;
+  const unsigned sub = lane & 7u;
+  const uint64_t S = scr.map_size, smask = S - 1;
   unsigned long long n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0;  // lane 0 only
 
   for (uint64_t b = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nb;
        b += nwarps) {
-    const uint32_t g = scr.cnt[b];
-    if (g == 0) continue;
-    const uint32_t o = scr.off[b];
+    if (!scr.mark[b]) continue;  // no key of the batch here
     const uint64_t base = b * kSlots + lane * 4;
+    // This bucket's stage run: from lo, past a_end, up to the first free
+    // position at or after a_end (linear probing leaves no gap in a run).
+    const uint64_t lo = area_start(b, S, nb, scr.area_shift);
+    const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
 
-    uint64_t sk[4], sc[4];
-    uint32_t occ[4] = {kNone, kNone, kNone, kNone};
-    uint32_t fresh = 0;
-    {
-      const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(t.keys + base);
-      const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(t.keys + base + 2);
-      sk[0] = a.x; sk[1] = a.y; sk[2] = c.x; sk[3] = c.y;
+    // Loads: the bucket (the lane's four key/score pairs and digest bytes)
+    // and the first kWin chunks of the run, all issued before any use.
+    ulonglong2 kv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) kv[q] = *reinterpret_cast<const ulonglong2*>(key_at(t, base + q));
+    const uint32_t dw = *reinterpret_cast<const uint32_t*>(t.digests + base);
+    const uint64_t nw_need = (a_end - lo) / 32 + 1;
+    const uint32_t nw = nw_need < kWin ? static_cast<uint32_t>(nw_need) : kWin;
+    uint64_t wk[kWin];
+    uint32_t wr[kWin];
+#pragma unroll
+    for (int w = 0; w < kWin; ++w) {
+      wk[w] = kEmptyKey;
+      wr[w] = 0;
+      if (w < static_cast<int>(nw)) {
+        const uint64_t j = (lo + 32ull * w + lane) & smask;
+        wk[w] = scr.map_keys[j];
+        wr[w] = scr.map_idx[j];
+      }
     }
-    bool have_scores = false;
-    const bool small = g <= 32;
-    // Entry registers of the first chunk are kept for the small case.
-    uint32_t e0 = kNone;
-    uint64_t k0 = kEmptyKey, s0 = 0;
-    bool hit0 = false;
+    *reinterpret_cast<ulonglong2*>(&st.key[lane * 4]) = make_ulonglong2(kv[0].x, kv[1].x);
+    *reinterpret_cast<ulonglong2*>(&st.key[lane * 4 + 2]) = make_ulonglong2(kv[2].x, kv[3].x);
+    *reinterpret_cast<ulonglong2*>(&st.score[lane * 4]) = make_ulonglong2(kv[0].y, kv[1].y);
+    *reinterpret_cast<ulonglong2*>(&st.score[lane * 4 + 2]) = make_ulonglong2(kv[2].y, kv[3].y);
+    *reinterpret_cast<uint4*>(&st.occ[lane * 4]) = make_uint4(kNone, kNone, kNone, kNone);
+    st.dig[lane] = dw;
+    if (lane < 4) st.fresh[lane] = 0;
 
-    // Phase A: keys already resident are updated in place (Algorithm 2,
-    // found branch).  All updates happen before any placement.
-    for (uint32_t c0 = 0; c0 < g; c0 += 32) {
-      const uint32_t e = (c0 + lane < g) ? scr.group[o + c0 + lane] : kNone;
-      const uint64_t ke = (e != kNone) ? keys_in[e] : kEmptyKey;
-      const uint64_t se = (e != kNone) ? (scores_in ? scores_in[e] : step_score) : 0;
-      const uint32_t cn = min(32u, g - c0);
-      bool myhit = false;
-      for (uint32_t j = 0; j < cn; ++j) {
-        const uint64_t kj = __shfl_sync(0xFFFFFFFFu, ke, j);
-        int qh = -1;
+    // Entry of chunk c for this lane: batch index if the stage position holds
+    // a key of bucket b before the end of the run (else kNone).  `stop`
+    // carries the run end across chunks.
+    bool run_ended = false;
+    auto entry_of = [&](uint64_t c, uint64_t key, uint32_t raw) -> uint32_t {
+      const uint64_t j = lo + 32ull * c + lane;
+      const bool empty = key == kEmptyKey;
+      const unsigned stopm = __ballot_sync(0xFFFFFFFFu, empty && j >= a_end);
+      const bool before = !run_ended && (stopm == 0 || lane < static_cast<unsigned>(__ffs(stopm) - 1));
+      if (stopm) run_ended = true;
+      if (32ull * (c + 1) >= S) run_ended = true;
+      const bool mine = !empty && before && bucket_of_hash(t, hash64(key)) == b;
+      return mine ? (raw & ~kHitMark) - 1 : kNone;
+    };
+    uint32_t we[kWin];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (sk[q] == kj) qh = q;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, qh >= 0);
-        if (m) {
-          const uint64_t sj = __shfl_sync(0xFFFFFFFFu, se, j);
-          const uint32_t ej = __shfl_sync(0xFFFFFFFFu, e, j);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (q == qh) {
-              occ[q] = ej;
-              sc[q] = sj;
+    for (int w = 0; w < kWin; ++w) we[w] = w < static_cast<int>(nw) ? entry_of(w, wk[w], wr[w]) : kNone;
+    const bool in_window = run_ended;  // the run ends inside the loaded chunks
+    __syncwarp();
+
+    // Phase A (Algorithm 2, found branch): a resident key gets its new value
+    // and score.  The entry lane scans the staged digest line and confirms
+    // matches against the staged keys.  Returns whether the entry hit.
+    auto phase_a = [&](uint32_t e, uint64_t ke) -> bool {
+      int hs = -1;
+      if (e != kNone) {
+        const uint32_t pat = digest_of_hash(hash64(ke)) * 0x01010101u;
+#pragma unroll 1
+        for (int w4 = 0; w4 < kSlots / 16 && hs < 0; ++w4) {
+          const uint4 d4 = reinterpret_cast<const uint4*>(st.dig)[w4];
+          uint32_t m = byte_match4(d4.x, pat) | (byte_match4(d4.y, pat) << 4) |
+                       (byte_match4(d4.z, pat) << 8) | (byte_match4(d4.w, pat) << 12);
+          while (m) {
+            const int slot = w4 * 16 + __ffs(m) - 1;
+            m &= m - 1;
+            if (st.key[slot] == ke) {
+              hs = slot;
+              break;
             }
-          if (lane == j) myhit = true;
+          }
+        }
+        if (hs >= 0) {
+          st.occ[hs] = e;
+          st.score[hs] = scores_in ? scores_in[e] : step_score;
         }
       }
-      const unsigned hm = __ballot_sync(0xFFFFFFFFu, myhit);
+      const unsigned hm = __ballot_sync(0xFFFFFFFFu, hs >= 0);
       if (lane == 0) n_upd += __popc(hm);
-      if (small) {
-        e0 = e; k0 = ke; s0 = se; hit0 = myhit;
-      } else if (myhit) {
-        scr.group[o + c0 + lane] = e | kHitMark;
-      }
-    }
+      return hs >= 0;
+    };
 
-    // Phase B: absent keys (Algorithm 2, empty-slot / eviction / rejection).
-    bool min_valid = false;
-    uint64_t ms = 0, mk = 0;
-    uint32_t mslot = 0;
-    for (uint32_t c0 = 0; c0 < g; c0 += 32) {
-      uint32_t e;
-      uint64_t ke, se;
-      bool miss;
-      if (small) {
-        e = e0; ke = k0; se = s0; miss = (e0 != kNone) && !hit0;
-      } else {
-        const uint32_t raw = (c0 + lane < g) ? scr.group[o + c0 + lane] : kNone;
-        miss = raw != kNone && !(raw & kHitMark);
-        e = miss ? raw : kNone;
-        ke = miss ? keys_in[e] : kEmptyKey;
-        se = miss ? (scores_in ? scores_in[e] : step_score) : 0;
+    // Phase B (Algorithm 2, empty slot / eviction / rejection) for the absent
+    // keys of one chunk.  Free slots (in slot order) go to the first absent
+    // keys.  For the E absent keys left, applying Algorithm 2 to each in turn
+    // leaves the 128 highest ranks of (bucket entries + those keys), so the
+    // warp drops the E lowest-ranked of that union directly: E extractions of
+    // the union's minimum, each one warp arg-min over per-lane candidates (the
+    // lane's lowest remaining bucket entry, presorted, or its own absent key).
+    // Extracted absent keys are rejected; the absent keys left take the slots
+    // of the extracted entries.
+    uint32_t nfree = 0, used = 0;
+    auto phase_b = [&](uint32_t e, uint64_t ke, bool miss) {
+      const uint64_t se = miss ? (scores_in ? scores_in[e] : step_score) : 0;
+      const unsigned mm = __ballot_sync(0xFFFFFFFFu, miss);
+      if (!mm) return;
+      const uint32_t rank = used + __popc(mm & lanemask_lt());
+      if (miss && rank < nfree) {
+        const uint32_t slot = st.list[rank];
+        st.key[slot] = ke;
+        st.score[slot] = se;
+        st.occ[slot] = e;
+        atomicOr(&st.fresh[slot >> 5], 1u << (slot & 31));
       }
-      unsigned mm = __ballot_sync(0xFFFFFFFFu, miss);
-      while (mm) {
-        const int j = __ffs(mm) - 1;
-        mm &= mm - 1;
-        const uint64_t kj = __shfl_sync(0xFFFFFFFFu, ke, j);
-        const uint64_t sj = __shfl_sync(0xFFFFFFFFu, se, j);
-        const uint32_t ej = __shfl_sync(0xFFFFFFFFu, e, j);
-        // free slot: the first one in slot order
-        int qf = -1;
+      const uint32_t placed = min(static_cast<uint32_t>(__popc(mm)), nfree - used);
+      used += placed;
+      if (lane == 0) n_adm += placed;
+      bool pending = miss && rank >= nfree;  // this lane's absent key still competes
+      const unsigned em = __ballot_sync(0xFFFFFFFFu, pending);
+      if (!em) return;
+      const uint32_t E = __popc(em);
+      __syncwarp();
+      // The lane's four bucket entries sorted by rank (five compare-exchanges).
+      uint64_t rs[4], rk[4];
+      uint32_t rq[4];
 #pragma unroll
-        for (int q = 3; q >= 0; --q)
-          if (sk[q] == kEmptyKey) qf = q;
-        const unsigned fm = __ballot_sync(0xFFFFFFFFu, qf >= 0);
-        if (fm) {
-          if (lane == static_cast<unsigned>(__ffs(fm) - 1)) {
+      for (int q = 0; q < 4; ++q) {
+        rs[q] = st.score[lane * 4 + q];
+        rk[q] = st.key[lane * 4 + q];
+        rq[q] = lane * 4 + q;
+      }
+      auto cx = [&](int x, int y) {
+        if (rank_less(rs[y], rk[y], rs[x], rk[x])) {
+          const uint64_t ts = rs[x], tk = rk[x];
+          const uint32_t tq = rq[x];
+          rs[x] = rs[y]; rk[x] = rk[y]; rq[x] = rq[y];
+          rs[y] = ts; rk[y] = tk; rq[y] = tq;
+        }
+      };
+      cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
+      int head = 0;
+      uint32_t nev = 0;  // extracted bucket entries (their slots go to st.list)
+      for (uint32_t x = 0; x < E; ++x) {
+        uint64_t cs = ~0ull, ck = ~0ull;
+        bool cand_is_miss = false;
+        if (head < 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q == head) { cs = rs[q]; ck = rk[q]; }
+        }
+        if (pending && (head >= 4 || rank_less(se, ke, cs, ck))) {
+          cs = se; ck = ke; cand_is_miss = true;
+        }
+        unsigned sel_s, sel_k;
+        warp_min_u64(cs, true, sel_s);
+        warp_min_u64(ck, (sel_s >> lane) & 1u, sel_k);
+        const unsigned wl = __ffs(sel_k) - 1;
+        // 0: an absent key (rejected); 1: a pre-call resident (evicted);
+        // 2: a key admitted earlier in this call (now counts as rejected)
+        uint32_t kind = 0;
+        if (lane == wl) {
+          if (cand_is_miss) {
+            pending = false;
+          } else {
+            uint32_t slot = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (q == qf) {
-                sk[q] = kj; sc[q] = sj; occ[q] = ej; fresh |= 1u << q;
-              }
+              if (q == head) slot = rq[q];
+            st.list[nev] = static_cast<uint8_t>(slot);
+            kind = (st.fresh[slot >> 5] & (1u << (slot & 31))) ? 2u : 1u;
+            ++head;
           }
-          if (lane == 0) ++n_adm;
-          continue;
         }
-        // bucket full: lowest-ranked entry (loaded once per bucket)
-        if (!have_scores) {
-          const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(t.scores + base);
-          const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(t.scores + base + 2);
-          const uint64_t ld[4] = {a.x, a.y, c.x, c.y};
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (occ[q] == kNone) sc[q] = ld[q];
-          have_scores = true;
-        }
-        if (!min_valid) {
-          uint64_t bs = sc[0], bk = sk[0];
-          uint32_t bslot = lane * 4;
-#pragma unroll
-          for (int q = 1; q < 4; ++q)
-            if (rank_less(sc[q], sk[q], bs, bk)) { bs = sc[q]; bk = sk[q]; bslot = lane * 4 + q; }
-          for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
-            const uint64_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-            const uint32_t osl = __shfl_xor_sync(0xFFFFFFFFu, bslot, off);
-            if (rank_less(os, ok, bs, bk)) { bs = os; bk = ok; bslot = osl; }
-          }
-          ms = bs; mk = bk; mslot = bslot;
-          min_valid = true;
-        }
-        if (rank_less(sj, kj, ms, mk)) {  // admission control
-          if (lane == 0) ++n_rej;
-          continue;
-        }
-        // evict the minimum
-        bool was_fresh = false;
-        if (lane == (mslot >> 2)) {
-          const int qv = static_cast<int>(mslot & 3);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (q == qv) {
-              was_fresh = (fresh >> q) & 1u;
-              sk[q] = kj; sc[q] = sj; occ[q] = ej; fresh |= 1u << q;
-            }
-        }
-        was_fresh = __shfl_sync(0xFFFFFFFFu, was_fresh, mslot >> 2);
+        kind = __shfl_sync(0xFFFFFFFFu, kind, wl);
+        if (kind) ++nev;
         if (lane == 0) {
-          if (was_fresh) ++n_rej;   // displaced a key admitted by this call
-          else { ++n_evi; ++n_adm; }
+          if (kind == 1) ++n_evi;
+          else if (kind == 2) { --n_adm; ++n_rej; }
+          else ++n_rej;
         }
-        min_valid = false;
       }
-    }
+      __syncwarp();
+      // absent keys still pending take the extracted slots
+      const unsigned am = __ballot_sync(0xFFFFFFFFu, pending);
+      if (pending) {
+        const uint32_t slot = st.list[__popc(am & lanemask_lt())];
+        st.key[slot] = ke;
+        st.score[slot] = se;
+        st.occ[slot] = e;
+        atomicOr(&st.fresh[slot >> 5], 1u << (slot & 31));
+      }
+      if (lane == 0) n_adm += __popc(am);
+      __syncwarp();
+    };
 
-    // Write back keys, digests and scores of the lane's slots, and queue the
-    // value copies of the final occupants.
-    uint32_t dirty = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (occ[q] != kNone) dirty |= 1u << q;
-    if (dirty) {
-      *reinterpret_cast<ulonglong2*>(t.keys + base) = make_ulonglong2(sk[0], sk[1]);
-      *reinterpret_cast<ulonglong2*>(t.keys + base + 2) = make_ulonglong2(sk[2], sk[3]);
-      uint32_t dw = 0;
+    auto build_free_list = [&]() {
+      uint32_t fm = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (sk[q] != kEmptyKey) dw |= digest_of_hash(hash64(sk[q])) << (8 * q);
-      *reinterpret_cast<uint32_t*>(t.digests + base) = dw;
-      if (have_scores) {
-        *reinterpret_cast<ulonglong2*>(t.scores + base) = make_ulonglong2(sc[0], sc[1]);
-        *reinterpret_cast<ulonglong2*>(t.scores + base + 2) = make_ulonglong2(sc[2], sc[3]);
-      } else {
+        if (st.key[lane * 4 + q] == kEmptyKey) fm |= 1u << q;
+      uint32_t pos = prefix_small(__popc(fm), nfree);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (occ[q] != kNone) t.scores[base + q] = sc[q];
+      for (int q = 0; q < 4; ++q)
+        if (fm & (1u << q)) st.list[pos++] = static_cast<uint8_t>(lane * 4 + q);
+      __syncwarp();
+    };
+
+    if (in_window) {
+      // Compact the window's entries, then work on dense chunks of 32.
+      uint32_t ne = 0;
+#pragma unroll
+      for (int w = 0; w < kWin; ++w) {
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, we[w] != kNone);
+        if (we[w] != kNone) {
+          const uint32_t p = ne + __popc(m & lanemask_lt());
+          st.ekey[p] = wk[w];
+          st.eidx[p] = we[w];
+        }
+        ne += __popc(m);
+      }
+      __syncwarp();
+      bool hit[kWin];
+#pragma unroll
+      for (int c = 0; c < kWin; ++c) {
+        hit[c] = false;
+        if (32u * c < ne) {
+          const bool v = 32u * c + lane < ne;
+          hit[c] = phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey);
+        }
+      }
+      __syncwarp();
+      build_free_list();
+#pragma unroll
+      for (int c = 0; c < kWin; ++c) {
+        if (32u * c < ne) {
+          const bool v = 32u * c + lane < ne;
+          const uint32_t e = v ? st.eidx[32 * c + lane] : kNone;
+          phase_b(e, v ? st.ekey[32 * c + lane] : kEmptyKey, v && !hit[c]);
+        }
+      }
+    } else {
+      // Long run: walk it chunk by chunk from the stage, marking hits there.
+      uint64_t nch = 0;
+      run_ended = false;
+      for (uint64_t c = 0; !run_ended; ++c) {
+        const uint64_t j = (lo + 32ull * c + lane) & smask;
+        const uint64_t key = scr.map_keys[j];
+        const uint32_t raw = scr.map_idx[j];
+        const uint32_t e = entry_of(c, key, raw);
+        if (phase_a(e, key)) scr.map_idx[j] = raw | kHitMark;
+        nch = c + 1;
+      }
+      __syncwarp();
+      build_free_list();
+      run_ended = false;
+      for (uint64_t c = 0; c < nch; ++c) {
+        const uint64_t j = (lo + 32ull * c + lane) & smask;
+        const uint64_t key = scr.map_keys[j];
+        const uint32_t raw = scr.map_idx[j];
+        const uint32_t e = entry_of(c, key, raw);
+        phase_b(e, key, e != kNone && !(raw & kHitMark));
       }
     }
-    const uint32_t nd = __popc(dirty);
-    uint32_t pos = nd;
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, pos, off);
-      if (lane >= static_cast<unsigned>(off)) pos += v;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, pos, 31);
-    pos -= nd;
+    __syncwarp();
+
+    // Phase C: write back the lane's changed slots and digest bytes, then
+    // copy the value rows of the final occupants.
+    uint32_t dm = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (occ[q] != kNone) jobs[pos++] = CopyJob{occ[q], lane * 4 + static_cast<uint32_t>(q)};
+      if (st.occ[lane * 4 + q] != kNone) dm |= 1u << q;
+    if (dm) {
+      uint32_t nd = dw;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!(dm & (1u << q))) continue;
+        const uint64_t k = st.key[lane * 4 + q];
+        *reinterpret_cast<ulonglong2*>(key_at(t, base + q)) =
+            make_ulonglong2(k, st.score[lane * 4 + q]);
+        nd = (nd & ~(0xFFu << (8 * q))) | (digest_of_hash(hash64(k)) << (8 * q));
+      }
+      *reinterpret_cast<uint32_t*>(t.digests + base) = nd;
+    }
+    uint32_t total;
+    uint32_t pos = prefix_small(__popc(dm), total);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (dm & (1u << q)) st.list[pos++] = static_cast<uint8_t>(lane * 4 + q);
     __syncwarp();
-    const unsigned sub = lane & 7u;
-    for (uint32_t p = lane >> 3; p < total; p += 4) {
-      const CopyJob jb = jobs[p];
-      tile_copy_row(row_ptr(t, b * kSlots + jb.slot),
-                    values_in + static_cast<uint64_t>(jb.src) * t.dim, t.dim, sub, vec, true);
+    // four rows per tile per pass, loads in flight together
+    for (uint32_t p0 = lane >> 3; p0 < total; p0 += 16) {
+      float* dst[4];
+      const float* src[4];
+      bool ok[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t p = p0 + 4 * r;
+        ok[r] = p < total;
+        const uint32_t slot = ok[r] ? st.list[p] : 0;
+        dst[r] = row_ptr(t, b * kSlots + slot);
+        src[r] = values_in + static_cast<uint64_t>(ok[r] ? st.occ[slot] : 0) * t.dim;
+      }
+      tile_copy_rows<4>(dst, src, ok, t.dim, sub, vec);
     }
     __syncwarp();
   }
@@ -395,7 +572,7 @@ __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
       const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
       tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
       if (sub == 0) {
-        t.scores[row] = scores ? scores[i] : step_score;
+        *score_at(t, row) = scores ? scores[i] : step_score;
         ++upd;
       }
     } else if (sub == 0) {
@@ -474,8 +651,8 @@ __global__ void __launch_bounds__(kThreads) dual_place_kernel(
     uint64_t k1[4], k2[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      k1[q] = ld_cg_u64(t.keys + b1 * kSlots + lane * 4 + q);
-      k2[q] = ld_cg_u64(t.keys + b2 * kSlots + lane * 4 + q);
+      k1[q] = ld_cg_u64(key_at(t, b1 * kSlots + lane * 4 + q));
+      k2[q] = ld_cg_u64(key_at(t, b2 * kSlots + lane * 4 + q));
     }
     int f1 = -1, f2 = -1, c1 = 0, c2 = 0;
 #pragma unroll
@@ -504,8 +681,8 @@ __global__ void __launch_bounds__(kThreads) dual_place_kernel(
       uint64_t s1[4], s2[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        s1[q] = ld_cg_u64(t.scores + b1 * kSlots + lane * 4 + q);
-        s2[q] = ld_cg_u64(t.scores + b2 * kSlots + lane * 4 + q);
+        s1[q] = ld_cg_u64(score_at(t, b1 * kSlots + lane * 4 + q));
+        s2[q] = ld_cg_u64(score_at(t, b2 * kSlots + lane * 4 + q));
       }
       uint64_t ms1, mk1, ms2, mk2;
       const uint32_t m1 = warp_argmin(s1, k1, ms1, mk1);
@@ -520,8 +697,8 @@ __global__ void __launch_bounds__(kThreads) dual_place_kernel(
     if (tslot >= 0) {
       const uint64_t row = tb * kSlots + static_cast<uint64_t>(tslot);
       if (lane == 0) {
-        t.keys[row] = k;
-        t.scores[row] = s;
+        *key_at(t, row) = k;
+        *score_at(t, row) = s;
         t.digests[row] = static_cast<uint8_t>(digest_of_hash(h));
       }
       float* dst = row_ptr(t, row);
@@ -616,7 +793,7 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScr
     const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
     tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
     if (sub == 0) {
-      if (scores) t.scores[row] = scores[i];
+      if (scores) *score_at(t, row) = scores[i];
       ++upd;
     }
   }
@@ -648,9 +825,8 @@ __global__ void __launch_bounds__(kThreads) erase_kernel(TableView t, uint64_t n
     if (slot >= 0 && sub == 0) {
       const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
       // Duplicates of k in the batch race here; exactly one CAS wins.
-      if (atomicCAS(reinterpret_cast<unsigned long long*>(t.keys + row), k, kEmptyKey) == k) {
+      if (atomicCAS(reinterpret_cast<unsigned long long*>(key_at(t, row)), k, kEmptyKey) == k) {
         t.digests[row] = 0;
-        t.scores[row] = 0;
         ++erased;
       }
     }
@@ -681,37 +857,49 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
-size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, bool need_groups) {
-  const uint64_t m = next_pow2(n * 2 < 64 ? 64 : n * 2);
+namespace {
+uint64_t stage_entries(uint64_t n) { return next_pow2(n * 2 < 64 ? 64 : n * 2); }
+}  // namespace
+
+size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind) {
+  const uint64_t m = stage_entries(n);
   size_t bytes = align256(m * 8) + align256(m * 4) + align256(64);
-  if (need_groups) bytes += 3 * align256(n * 4) + 2 * align256(num_buckets * 4);
+  if (kind == ScratchKind::kSingleUpsert) bytes += align256(num_buckets);
+  if (kind == ScratchKind::kDualUpsert) bytes += align256(n * 4);
   return bytes;
 }
 
-UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, bool need_groups) {
+UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind) {
   UpsertScratch s{};
-  const uint64_t m = next_pow2(n * 2 < 64 ? 64 : n * 2);
+  const uint64_t m = stage_entries(n);
   char* p = static_cast<char*>(base);
   s.map_size = static_cast<uint32_t>(m);
+  s.area_shift = kNoShift;
+  if ((num_buckets & (num_buckets - 1)) == 0) {
+    int lb = 0, lm = 0;
+    while ((1ull << lb) < num_buckets) ++lb;
+    while ((1ull << lm) < m) ++lm;
+    s.area_shift = lm - lb;
+  }
   s.map_keys = reinterpret_cast<uint64_t*>(p); p += align256(m * 8);
   s.map_idx = reinterpret_cast<uint32_t*>(p); p += align256(m * 4);
   s.cursor = reinterpret_cast<uint32_t*>(p); p += align256(64);
-  if (need_groups) {
-    s.bkt = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
-    s.rnk = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
+  if (kind == ScratchKind::kSingleUpsert) {
+    s.mark = reinterpret_cast<uint8_t*>(p); p += align256(num_buckets);
+  }
+  if (kind == ScratchKind::kDualUpsert) {
     s.group = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
-    s.cnt = reinterpret_cast<uint32_t*>(p); p += align256(num_buckets * 4);
-    s.off = reinterpret_cast<uint32_t*>(p); p += align256(num_buckets * 4);
   }
   return s;
 }
 
-cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, bool need_groups,
+cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(s.map_keys, 0xFF, static_cast<size_t>(s.map_size) * 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s.map_idx, 0, static_cast<size_t>(s.map_size) * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s.cursor, 0, 64, st);
-  if (e == cudaSuccess && need_groups) e = cudaMemsetAsync(s.cnt, 0, num_buckets * 4, st);
+  if (e == cudaSuccess && kind == ScratchKind::kSingleUpsert)
+    e = cudaMemsetAsync(s.mark, 0, num_buckets, st);
   return e;
 }
 
@@ -720,14 +908,13 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
                           uint64_t step_score, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
-  dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, t.stats);
   if (!t.dual) {
-    group_count_kernel<<<grid_for(n), kThreads, 0, st>>>(t, s, n, keys);
-    group_offsets_kernel<<<grid_for(t.num_buckets), kThreads, 0, st>>>(s, t.num_buckets);
-    group_scatter_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n);
-    upsert_single_kernel<<<grid_for(t.num_buckets * 32), kThreads, 0, st>>>(
+    stage_kernel<<<grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread), kThreads, 0,
+                   st>>>(t, s, n, keys);
+    upsert_single_kernel<<<grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS), kThreads, 0, st>>>(
         t, s, keys, values, scores, step_score, vec);
   } else {
+    dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, t.stats);
     dual_resident_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, scores,
                                                                 step_score, vec);
     dual_place_kernel<<<grid_for(n * 32), kThreads, 0, st>>>(t, s, keys, values, scores, step_score,

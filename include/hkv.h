@@ -178,12 +178,13 @@ hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
  * serving loop must never enter cudaMalloc/cudaFree (which can synchronise
  * the device).  It calls no allocation routine.
  *  - Limit: the batch's working memory must fit the array, i.e.
- *      a(8M) + a(4M) + 256 + (single mode only) 3 a(4n) + 2 a(4B) bytes,
+ *      a(8M) + a(4M) + 256 + a(B) bytes in single mode and
+ *      a(8M) + a(4M) + 256 + a(4n) bytes in dual mode,
  *    with M the smallest power of two >= max(64, 2n), B the bucket count and
  *    a(x) = x rounded up to a multiple of 256.  Larger batches return
  *    HKV_ERR_INVALID and enqueue nothing (split them, or use
- *    hkv_insert_or_assign).  Single mode with 32,768 buckets takes up to
- *    2^19 keys per call.
+ *    hkv_insert_or_assign).  Single mode takes up to 2^20 keys per call for
+ *    tables of up to 2^23 buckets.
  *  - Sharing: every call on every table of a device uses the same array and
  *    clears it before use.  Calls whose kernels overlap on the GPU (on
  *    different streams, from any table) race on it and corrupt each other's

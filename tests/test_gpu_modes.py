@@ -1,0 +1,207 @@
+"""GPU checks of dual-bucket mode (invariants, since placement depends on the
+order the GPU processes absent keys), tiered mode (bit-exact against an
+HBM-only twin) and reader/updater/inserter ordering across streams (bit-exact
+against the oracle's serial replay in host issue order)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, find_compare, table_state, u64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hkv():
+    import hash_table_cache_gb300 as m
+    from hash_table_cache_gb300 import _build
+    _build.build()
+    m.load()
+    return m
+
+
+@pytest.fixture(scope="module")
+def oracle_mod():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def _slots_state(t):
+    """(keys, scores, bucket of the slot) of every resident entry: one export
+    per bucket, so each entry's bucket is known."""
+    ks, ss, bs = [], [], []
+    for b in range(t.num_buckets):
+        kb, _, sb = t.export(b * 128, b * 128 + 128, with_values=False)
+        kb = u64(kb)
+        ks.append(kb)
+        ss.append(u64(sb))
+        bs.append(np.full(kb.size, b, np.uint64))
+    return np.concatenate(ks), np.concatenate(ss), np.concatenate(bs)
+
+
+def _check_dual_invariants(t, o, last_score, last_salt, dim, absent_ok=True):
+    keys, scores, buckets = _slots_state(t)
+    assert np.unique(keys).size == keys.size, "duplicate keys"
+    assert np.bincount(buckets.astype(np.int64), minlength=t.num_buckets).max() <= 128
+    b1 = o.buckets_of(keys, 0)
+    b2 = o.buckets_of(keys, 1)
+    assert np.all((buckets == b1) | (buckets == b2)), "key outside its two candidate buckets"
+    # every resident entry carries its last presentation
+    want_s = np.array([last_score[int(k)] for k in keys], np.uint64)
+    assert np.array_equal(scores, want_s)
+    vk, vv, _ = t.export()
+    torch.cuda.synchronize()
+    vk = u64(vk)
+    vv = vv.cpu().numpy()
+    for salt in np.unique([last_salt[int(k)] for k in vk[:2000]]):
+        sel = np.array([last_salt[int(k)] == salt for k in vk])
+        assert np.array_equal(vv[sel], wl.key_values(vk[sel], dim, salt=int(salt)))
+    # an absent key is outranked: one candidate bucket is full and its
+    # lowest rank is above the key's rank (scores never decrease here)
+    res = set(keys.tolist())
+    full = np.bincount(buckets.astype(np.int64), minlength=t.num_buckets) == 128
+    minrank = {}
+    for b in np.flatnonzero(full):
+        sel = buckets == b
+        j = np.lexsort((keys[sel], scores[sel]))[0]
+        minrank[int(b)] = (int(scores[sel][j]), int(keys[sel][j]))
+    absent = [k for k in last_score if k not in res]
+    for k in absent[:20000]:
+        r = (last_score[k], k)
+        c = [int(o.bucket(k, 0)), int(o.bucket(k, 1))]
+        assert any(cb in minrank and minrank[cb] > r for cb in c), (k, r, c)
+    return keys.size
+
+
+def test_dual_bucket_invariants(hkv, oracle_mod):
+    """Dual mode (HKV Algorithm 3): 1.5 x capacity unique keys with unique
+    random scores in batches, then an update batch raising scores; invariants
+    after every batch, find consistent with the table, and the retention of
+    the top-N scores reported beside the oracle's."""
+    B, dim, bs = 256, 8, 4096
+    cap = B * 128
+    t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_DUAL)
+    o = oracle_mod.OracleTable(B, dim, dual=True)
+    keys = wl.unique_keys(81, int(1.5 * cap))
+    scores = wl.stream(82, keys.size) >> np.uint64(2)
+    last_score, last_salt = {}, {}
+    for i, lo in enumerate(range(0, keys.size, bs)):
+        k, s = keys[lo:lo + bs], scores[lo:lo + bs]
+        v = wl.key_values(k, dim, salt=i)
+        t.reset_op_counts()
+        before = t.size()
+        t.insert_or_assign(dkeys(k), dvals(v), dkeys(s))
+        o.insert_or_assign(k, v, s)
+        for kk, ss in zip(k.tolist(), s.tolist()):
+            last_score[kk], last_salt[kk] = ss, i
+        c = t.op_counts()
+        assert c["admitted"] + c["rejected"] == k.size and c["updated"] == 0
+        assert t.size() == before + c["admitted"] - c["evicted"]
+        if i % 4 == 3:
+            _check_dual_invariants(t, o, last_score, last_salt, dim)
+    assert t.error_counts()["timeouts"] == 0
+    # updates with higher scores and new values
+    res = u64(t.export(with_values=False)[0])
+    up = res[:: 3]
+    new_s = np.array([last_score[int(x)] + 7 for x in up], np.uint64)
+    v = wl.key_values(up, dim, salt=999)
+    t.reset_op_counts()
+    t.insert_or_assign(dkeys(up), dvals(v), dkeys(new_s))
+    assert t.op_counts()["updated"] == up.size
+    for kk, ss in zip(up.tolist(), new_s.tolist()):
+        last_score[kk], last_salt[kk] = ss, 999
+    n_res = _check_dual_invariants(t, o, last_score, last_salt, dim)
+    # find agrees with the table contents
+    ek, ev, es = t.export()
+    torch.cuda.synchronize()
+    q = np.concatenate([keys, wl.unique_keys(83, 1000)])
+    fv, ff, fs = t.find(dkeys(q))
+    torch.cuda.synchronize()
+    ff = ff.cpu().numpy().astype(bool)
+    ek = u64(ek)
+    assert ff.sum() == n_res
+    pos = {k: i for i, k in enumerate(ek.tolist())}
+    idx = np.array([pos[int(x)] for x in q[ff]])
+    assert np.array_equal(fv.cpu().numpy()[ff], ev.cpu().numpy()[idx])
+    assert np.array_equal(u64(fs)[ff], u64(es)[idx])
+    # top-N retention (HKV Table 11), GPU and oracle
+    n_top = cap
+    top = {k for k, _ in sorted(last_score.items(), key=lambda kv: (kv[1], kv[0]))[-n_top:]}
+    gpu_ret = len(top & set(ek.tolist())) / n_top
+    ora_ret = len(top & set(o.export()[0].tolist())) / n_top
+    print(f"dual top-N retention: gpu {gpu_ret:.4f} oracle {ora_ret:.4f}")
+    assert gpu_ret > 0.95 and abs(gpu_ret - ora_ret) < 0.02
+
+
+def test_tiered_equals_hbm_only(hkv, oracle_mod):
+    """Tiered mode (HKV §3.6): with half of the value rows in mapped host
+    memory every result equals an HBM-only twin bit for bit."""
+    B, dim = 512, 16
+    cap = B * 128
+    budget = (B // 2) * 128 * 4 * dim
+    t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=budget)
+    h = hkv.HashTable(cap, dim)
+    assert t.info()["hbm_value_rows"] == cap // 2
+    keys = wl.unique_keys(91, 2 * cap)
+    for i, lo in enumerate(range(0, keys.size, 16384)):
+        k = keys[lo:lo + 16384]
+        v = dvals(wl.key_values(k, dim, salt=i))
+        for x in (t, h):
+            x.insert_or_assign(dkeys(k), v, None)
+        if i % 3 == 2:
+            a = dkeys(k[::5])
+            av = dvals(wl.key_values(k[::5], dim, salt=100 + i))
+            for x in (t, h):
+                x.assign(a, av, None)
+    for x, y in zip(table_state(t), table_state(h)):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    q = dkeys(np.concatenate([keys[::3], wl.unique_keys(92, 5000)]))
+    a = t.find(q)
+    b = h.find(q)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_roles_across_streams(hkv, oracle_mod):
+    """insert_or_assign, find and assign issued on three streams in a fixed
+    host order give exactly the oracle's serial replay in that order (HKV
+    §3.5 Table 4: conflicting roles never overlap)."""
+    B, dim = 64, 8
+    cap = B * 128
+    t = hkv.HashTable(cap, dim)
+    o = oracle_mod.OracleTable(B, dim)
+    s_ins, s_find, s_upd = (torch.cuda.Stream() for _ in range(3))
+    universe = wl.unique_keys(95, 3 * cap)
+    rng = np.random.default_rng(5)
+    plan = []
+    for step in range(12):  # inputs first, all on the device before any call
+        k = universe[rng.integers(0, universe.size, 4000)]
+        v = wl.key_values(k, dim, salt=step)
+        q = universe[rng.integers(0, universe.size, 3000)]
+        a = universe[rng.integers(0, universe.size, 2000)]
+        av = wl.key_values(a, dim, salt=1000 + step)
+        out = (torch.full((q.size, dim), -1.0, device=DEV),
+               torch.zeros(q.size, dtype=torch.uint8, device=DEV),
+               torch.zeros(q.size, dtype=torch.int64, device=DEV))
+        plan.append((k, v, dkeys(k), dvals(v), q, dkeys(q), out, a, av, dkeys(a), dvals(av)))
+    torch.cuda.synchronize()
+    # issue without host synchronisation: only the library's role events
+    # order the three streams
+    for (k, v, dk, dv, q, dq, out, a, av, da, dav) in plan:
+        t.insert_or_assign(dk, dv, None, stream=s_ins)
+        t.find(dq, *out, stream=s_find)
+        t.assign(da, dav, None, stream=s_upd)
+    torch.cuda.synchronize()
+    for (k, v, dk, dv, q, dq, out, a, av, da, dav) in plan:
+        o.insert_or_assign(k, v, None)
+        ov, of, os_ = o.find(q, values_out=np.full((q.size, dim), -1.0, np.float32),
+                             scores_out=np.zeros(q.size, np.uint64))
+        gv, gf, gs = out
+        assert np.array_equal(gf.cpu().numpy(), of)
+        assert np.array_equal(gv.cpu().numpy(), ov)
+        assert np.array_equal(u64(gs), os_)
+        o.assign(a, av, None)
+    assert_same_state(t, o)
