@@ -18,7 +18,8 @@ struct UpsertScratch {
   int32_t area_shift;   // single mode, power-of-two bucket count B: log2(S/B)
                         // (negative: B > S); kNoShift otherwise
   uint32_t* cursor;     // small counters (0-initialised)
-  uint8_t* mark;        // single mode: one byte per table bucket, 1 = holds batch keys
+  uint8_t* mark;        // single mode, sparse batches: one byte per table bucket,
+                        // 1 = holds batch keys (null for dense batches)
   uint32_t* group;      // dual mode: indices of the batch's absent keys
 };
 

@@ -158,7 +158,10 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
         pv = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + p), kEmptyKey, k[u]);
       }
       atomicMax(sc.map_idx + p, static_cast<uint32_t>(i0 + u * stride) + 1);
-      sc.mark[b[u]] = 1;  // the bucket holds keys of the batch (plain store)
+      // Sparse batches mark the buckets they touch (plain store) so that the
+      // processing kernel skips the others without reading them; dense
+      // batches skip the marks, which would only collide.
+      if (sc.mark) sc.mark[b[u]] = 1;
     }
   }
   warp_add(&t.stats->reserved, reserved);
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
 
   for (uint64_t b = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nb;
        b += nwarps) {
-    if (!scr.mark[b]) continue;  // no key of the batch here
+    if (scr.mark && !scr.mark[b]) continue;  // no key of the batch here
     const uint64_t base = b * kSlots + lane * 4;
     // This bucket's stage run: from lo, past a_end, up to the first free
     // position at or after a_end (linear probing leaves no gap in a run).
@@ -368,46 +371,69 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         }
       };
       cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
+      // 32-bit keys that preserve the rank order (ties allowed): the score
+      // relative to the union's minimum, with the top 16 key bits appended
+      // when the scores span less than 2^16, shifted right when they span
+      // more than 2^32.  Each extraction is then one 32-bit warp reduction;
+      // lanes tied on it are resolved exactly.
+      unsigned sel;
+      const uint64_t smin = warp_min_u64(pending && rank_less(se, ke, rs[0], rk[0]) ? se : rs[0],
+                                         true, sel);
+      const uint64_t smax = ~warp_min_u64(~((pending && se > rs[3]) ? se : rs[3]), true, sel);
+      const uint64_t span = smax - smin;
+      const int sh = span >> 32 ? 32 - __clzll(static_cast<long long>(span)) : 0;
+      auto fkey = [&](uint64_t sc, uint64_t k) -> uint32_t {
+        if (span < 65536) return static_cast<uint32_t>(((sc - smin) << 16) | (k >> 48));
+        return static_cast<uint32_t>((sc - smin) >> sh);
+      };
+      uint32_t rf[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rf[q] = fkey(rs[q], rk[q]);
+      const uint32_t mf = pending ? fkey(se, ke) : 0xFFFFFFFFu;
       int head = 0;
-      uint32_t nev = 0;  // extracted bucket entries (their slots go to st.list)
       for (uint32_t x = 0; x < E; ++x) {
-        uint64_t cs = ~0ull, ck = ~0ull;
-        bool cand_is_miss = false;
-        if (head < 4) {
+        uint32_t hf = 0xFFFFFFFFu;
+        uint64_t hs = ~0ull, hk = ~0ull;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (q == head) { cs = rs[q]; ck = rk[q]; }
+        for (int q = 0; q < 4; ++q)
+          if (q == head) { hf = rf[q]; hs = rs[q]; hk = rk[q]; }
+        const bool take_miss =
+            pending && (mf < hf || (mf == hf && rank_less(se, ke, hs, hk)));
+        const uint32_t lf = take_miss ? mf : hf;
+        const uint32_t m = __reduce_min_sync(0xFFFFFFFFu, lf);
+        const unsigned tied = __ballot_sync(0xFFFFFFFFu, lf == m);
+        unsigned wl = __ffs(tied) - 1;
+        if (tied & (tied - 1)) {  // several lanes share the 32-bit key: exact rank
+          const uint64_t cs = take_miss ? se : hs, ck = take_miss ? ke : hk;
+          unsigned sel_s, sel_k;
+          warp_min_u64(cs, (tied >> lane) & 1u, sel_s);
+          warp_min_u64(ck, (sel_s >> lane) & 1u, sel_k);
+          wl = __ffs(sel_k) - 1;
         }
-        if (pending && (head >= 4 || rank_less(se, ke, cs, ck))) {
-          cs = se; ck = ke; cand_is_miss = true;
-        }
-        unsigned sel_s, sel_k;
-        warp_min_u64(cs, true, sel_s);
-        warp_min_u64(ck, (sel_s >> lane) & 1u, sel_k);
-        const unsigned wl = __ffs(sel_k) - 1;
-        // 0: an absent key (rejected); 1: a pre-call resident (evicted);
-        // 2: a key admitted earlier in this call (now counts as rejected)
-        uint32_t kind = 0;
         if (lane == wl) {
-          if (cand_is_miss) {
-            pending = false;
-          } else {
-            uint32_t slot = 0;
+          if (take_miss) pending = false;  // rejected
+          else ++head;                      // that entry leaves the bucket
+        }
+      }
+      // The lane's extracted entries are its first `head` sorted slots.
+      uint32_t n_ext;
+      uint32_t pos = prefix_small(static_cast<uint32_t>(head), n_ext);
+      uint32_t ev = 0, fr = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (q == head) slot = rq[q];
-            st.list[nev] = static_cast<uint8_t>(slot);
-            kind = (st.fresh[slot >> 5] & (1u << (slot & 31))) ? 2u : 1u;
-            ++head;
-          }
+      for (int q = 0; q < 4; ++q) {
+        if (q < head) {
+          const uint32_t slot = rq[q];
+          st.list[pos++] = static_cast<uint8_t>(slot);
+          if (st.fresh[slot >> 5] & (1u << (slot & 31))) ++fr;  // admitted earlier this call
+          else ++ev;                                             // pre-call resident
         }
-        kind = __shfl_sync(0xFFFFFFFFu, kind, wl);
-        if (kind) ++nev;
-        if (lane == 0) {
-          if (kind == 1) ++n_evi;
-          else if (kind == 2) { --n_adm; ++n_rej; }
-          else ++n_rej;
-        }
+      }
+      const uint32_t n_ev = __reduce_add_sync(0xFFFFFFFFu, ev);
+      const uint32_t n_fr = __reduce_add_sync(0xFFFFFFFFu, fr);
+      if (lane == 0) {
+        n_evi += n_ev;
+        n_adm -= n_fr;
+        n_rej += n_fr + (E - n_ext);  // displaced fresh keys + rejected absent keys
       }
       __syncwarp();
       // absent keys still pending take the extracted slots
@@ -886,6 +912,7 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
   s.cursor = reinterpret_cast<uint32_t*>(p); p += align256(64);
   if (kind == ScratchKind::kSingleUpsert) {
     s.mark = reinterpret_cast<uint8_t*>(p); p += align256(num_buckets);
+    if (n >= 2 * num_buckets) s.mark = nullptr;  // dense batch: no marks
   }
   if (kind == ScratchKind::kDualUpsert) {
     s.group = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
@@ -898,7 +925,7 @@ cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, S
   cudaError_t e = cudaMemsetAsync(s.map_keys, 0xFF, static_cast<size_t>(s.map_size) * 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s.map_idx, 0, static_cast<size_t>(s.map_size) * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s.cursor, 0, 64, st);
-  if (e == cudaSuccess && kind == ScratchKind::kSingleUpsert)
+  if (e == cudaSuccess && kind == ScratchKind::kSingleUpsert && s.mark)
     e = cudaMemsetAsync(s.mark, 0, num_buckets, st);
   return e;
 }
