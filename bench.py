@@ -358,6 +358,171 @@ def run_gpu(args):
 
 
 # ---------------------------------------------------------------------------
+# The other workloads (measurement runs; the default line is the one above)
+# ---------------------------------------------------------------------------
+OTHER = {
+    "c1": "single-bucket, capacity 65,536, dim 8, one batch of 65,536 unique keys (score = index), "
+          "then a find of 65,536 keys (half inserted)",
+    "c3": "single-bucket, capacity 2^26, dim 64, load factor 1.0, steps of insert_or_assign 2^20 "
+          "Zipf(1.05) over 2^32 keys (score = step) + find 2^20 from the same Zipf",
+    "c4": "dual-bucket, capacity 2^26, dim 128, unique keys with unique random scores in 2^20 batches "
+          "(table full after the untimed prefill), + find 2^20 of the inserted keys",
+    "c5": "tiered single-bucket, capacity 2^28, dim 64, 32 GiB of values in HBM and 32 GiB in mapped "
+          "host memory, load factor 1.0; mixed stream on three CUDA streams: find 60%, assign 20%, "
+          "insert_or_assign 20%, batches of 2^20, Zipf(1.1) over 2^34 keys",
+}
+
+
+def run_other(args):
+    import torch
+
+    import hash_table_cache_gb300 as hkv
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    hkv.load()
+    cfg = args.config
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def dk(a):
+        return torch.from_numpy(wl.as_i64(np.asarray(a, np.uint64))).to(dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def prefill(t, dim, seed, batch=1 << 20, scores=False):
+        keys = wl.unique_keys(seed, int(1.6 * t.capacity))
+        pos = 0
+        while t.size() < t.capacity and pos < keys.size:
+            k = dk(keys[pos:pos + batch])
+            sc = dk(wl.stream(seed + 1, k.numel(), pos) >> np.uint64(2)) if scores else None
+            t.insert_or_assign(k, wl.key_values_torch(k, dim, salt=1), sc)
+            pos += batch
+        torch.cuda.synchronize()
+        return keys[:pos]
+
+    nsteps = args.warmup + args.steps
+    times, nkeys, launches = [], [], 0
+    if cfg == "c1":
+        cap, dim, n = 65536, 8, 65536
+        keys = wl.unique_keys(1, n)
+        vals = wl.randn_values(0, n, dim, device=dev)
+        sc = dk(np.arange(n, dtype=np.uint64))
+        q = np.empty(n, np.uint64)
+        q[0::2] = keys[0::2]
+        q[1::2] = wl.unique_keys(2, n // 2)
+        kd, qd = dk(keys), dk(q)
+        t = None
+        for s in range(nsteps):
+            if t is not None:
+                t.close()
+            t = hkv.HashTable(cap, dim)
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            t.insert_or_assign(kd, vals, sc)
+            t.find(qd)
+            b.record(stream)
+            b.synchronize()
+            if s >= args.warmup:
+                times.append(a.elapsed_time(b) * 1e-3)
+                nkeys.append(2 * n)
+        launches = 3
+    elif cfg == "c3":
+        cap, dim, n = 1 << 26, 64, 1 << 20
+        t = hkv.HashTable(cap, dim)
+        prefill(t, dim, 6)
+        z = wl.Zipf(1.05, 1 << 32)
+        for s in range(nsteps):
+            u = dk(wl.zipf_keys(7 + s, n, 1.05, 1 << 32))
+            f = dk(wl.zipf_keys(10007 + s, n, 1.05, 1 << 32))
+            uv = wl.key_values_torch(u, dim, salt=100 + s)
+            torch.cuda.synchronize()
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            t.insert_or_assign(u, uv, None)
+            t.find(f)
+            b.record(stream)
+            b.synchronize()
+            if s >= args.warmup:
+                times.append(a.elapsed_time(b) * 1e-3)
+                nkeys.append(2 * n)
+        launches = 3
+    elif cfg == "c4":
+        cap, dim, n = 1 << 26, 128, 1 << 20
+        t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_DUAL)
+        inserted = prefill(t, dim, 8, scores=True)
+        base = inserted.size
+        more = wl.unique_keys(9, nsteps * n)
+        for s in range(nsteps):
+            u = dk(more[s * n:(s + 1) * n])
+            usc = dk(wl.stream(90, n, s * n) >> np.uint64(2))
+            f = dk(wl.choice(10 + s, inserted, n))
+            uv = wl.key_values_torch(u, dim, salt=200 + s)
+            torch.cuda.synchronize()
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            t.insert_or_assign(u, uv, usc)
+            t.find(f)
+            b.record(stream)
+            b.synchronize()
+            if s >= args.warmup:
+                times.append(a.elapsed_time(b) * 1e-3)
+                nkeys.append(2 * n)
+        launches = 7
+    elif cfg == "c5":
+        cap, dim, n = 1 << 28, 64, 1 << 20
+        t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=32 << 30)
+        prefill(t, dim, 11)
+        sf, sa, su = (torch.cuda.Stream() for _ in range(3))
+        kinds = ["find", "find", "find", "assign", "upsert"]
+        plan = []
+        for s in range(nsteps * 5):
+            k = dk(wl.zipf_keys(12 + s, n, 1.1, 1 << 34))
+            plan.append((kinds[s % 5], k, wl.key_values_torch(k, dim, salt=0)))
+        outs = [(torch.empty((n, dim), device=dev), torch.empty(n, dtype=torch.uint8, device=dev))
+                for _ in range(3)]
+        torch.cuda.synchronize()
+        for s in range(nsteps):
+            a, b = ev(), ev()
+            flush.zero_()
+            a.record(stream)
+            for x, (kind, k, v) in enumerate(plan[5 * s:5 * s + 5]):
+                if kind == "find":
+                    t.find(k, outs[x][0], outs[x][1], None, with_scores=False, stream=sf)
+                elif kind == "assign":
+                    t.assign(k, v, None, stream=sa)
+                else:
+                    t.insert_or_assign(k, v, None, stream=su)
+            for st_ in (sf, sa, su):
+                e = torch.cuda.Event()
+                e.record(st_)
+                stream.wait_event(e)
+            b.record(stream)
+            b.synchronize()
+            if s >= args.warmup:
+                times.append(a.elapsed_time(b) * 1e-3)
+                nkeys.append(5 * n)
+        launches = 3 + 2 + 2
+    counts = t.op_counts()
+    total = sum(times)
+    line = {
+        "metric": METRIC, "value": sum(nkeys) / total / 1e9, "unit": "B-KV/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u64 keys/scores, f32 values (copied)", "data": "synthetic",
+        "config": {"workload": OTHER[cfg], "name": cfg,
+                   "l2": "flushed between steps (256 MiB write), flush outside timed events"},
+        "op_counts": counts, "gpu_launches": launches * args.steps,
+    }
+    t.close()
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (reported baseline, and the --impl reference arm)
 # ---------------------------------------------------------------------------
 SAMPLE_EVERY = 8  # the oracle simulates every 8th bucket of the table
@@ -452,9 +617,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-sweep", action="store_true", help="only the headline steps")
+    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"],
+                    help="workload; c2 (the default) is the headline line")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.config != "c2":
+        run_other(args)
     else:
         run_gpu(args)
 
