@@ -72,6 +72,9 @@ def _load():
         "oracle_assign": (None, [vp, u64, vp, vp, vp, ctypes.POINTER(_Counts)]),
         "oracle_erase": (None, [vp, u64, vp, ctypes.POINTER(_Counts)]),
         "oracle_find": (u64, [vp, u64, vp, vp, vp, vp]),
+        "oracle_insert_and_evict": (None, [vp, u64, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Counts)]),
+        "oracle_find_or_insert": (None, [vp, u64, vp, vp, vp, vp, ctypes.POINTER(_Counts)]),
+        "oracle_contains": (None, [vp, u64, vp, vp]),
         "oracle_size": (u64, [vp]),
         "oracle_bucket_size": (u64, [vp, u64]),
         "oracle_export": (u64, [vp, u64, u64, u64, vp, vp, vp]),
@@ -179,6 +182,38 @@ class OracleTable:
         found = np.zeros(n, np.uint8)
         _load().oracle_find(self._h, n, _ptr(k), _ptr(vals), _ptr(found), _ptr(scs))
         return vals, found, scs
+
+    def insert_and_evict(self, keys, values, scores=None):
+        """Returns (counts, (evicted keys, values, scores) sorted by key)."""
+        k = _keys(keys)
+        v = self._values(values, k.size)
+        s = None if scores is None else _keys(scores)
+        ek = np.zeros(max(k.size, 1), np.uint64)
+        ev = np.zeros((max(k.size, 1), self.dim), np.float32)
+        es = np.zeros(max(k.size, 1), np.uint64)
+        cnt = np.zeros(1, np.uint64)
+        c = _Counts()
+        _load().oracle_insert_and_evict(self._h, k.size, _ptr(k), _ptr(v), _ptr(s), _ptr(ek), _ptr(ev),
+                                        _ptr(es), _ptr(cnt), ctypes.byref(c))
+        m = int(cnt[0])
+        return c.as_dict(), (ek[:m], ev[:m], es[:m])
+
+    def find_or_insert(self, keys, values, scores=None):
+        """Returns (counts, values after the call, found flags)."""
+        k = _keys(keys)
+        v = self._values(values, k.size).copy().reshape(k.size, self.dim)
+        s = None if scores is None else _keys(scores)
+        found = np.zeros(k.size, np.uint8)
+        c = _Counts()
+        _load().oracle_find_or_insert(self._h, k.size, _ptr(k), _ptr(v), _ptr(s), _ptr(found),
+                                      ctypes.byref(c))
+        return c.as_dict(), v, found
+
+    def contains(self, keys):
+        k = _keys(keys)
+        found = np.zeros(k.size, np.uint8)
+        _load().oracle_contains(self._h, k.size, _ptr(k), _ptr(found))
+        return found
 
     def size(self) -> int:
         return int(_load().oracle_size(self._h))

@@ -160,9 +160,19 @@ struct Table {
     // Outcome of one absent key (HKV Algorithm 2 / 3 return values).
     enum Outcome { kInserted, kEvicted, kRejected };
 
+    // A displaced entry as it was at the moment of its displacement.
+    struct Victim { uint64_t key = 0, score = 0; std::vector<float> value; };
+
+    void take_victim(const Bucket& bk, int m, Victim* out) {
+        out->key = bk.keys[m];
+        out->score = bk.scores[m];
+        out->value.assign(bk.values.begin() + static_cast<long>(m) * dim,
+                          bk.values.begin() + static_cast<long>(m + 1) * dim);
+    }
+
     // HKV Algorithm 2, branches after the (failed) lookup, on bucket b.
-    // On kEvicted, *victim receives the displaced key.
-    Outcome insert_single(uint64_t b, uint64_t k, uint64_t s, const float* v, uint64_t* victim) {
+    // On kEvicted, *victim receives the displaced entry.
+    Outcome insert_single(uint64_t b, uint64_t k, uint64_t s, const float* v, Victim* victim) {
         Bucket& bk = at(b);
         if (bk.size() < kSlots) {                 // first empty slot exists
             append_entry(bk, k, s, v);
@@ -171,13 +181,13 @@ struct Table {
         int m = bk.argmin_rank();                 // bucket full: eviction path
         if (rank_less(s, k, bk.scores[m], bk.keys[m]))
             return kRejected;                     // admission control
-        *victim = bk.keys[m];
+        take_victim(bk, m, victim);
         write_entry(bk, m, k, s, v);              // replace the minimum
         return kEvicted;
     }
 
     // HKV Algorithm 3 (score-based dual-bucket upsert), for an absent key.
-    Outcome insert_dual(uint64_t k, uint64_t s, const float* v, uint64_t* victim) {
+    Outcome insert_dual(uint64_t k, uint64_t s, const float* v, Victim* victim) {
         uint64_t b1 = bucket1(k), b2 = bucket2(k);
         Bucket& x = at(b1);
         Bucket& y = at(b2);
@@ -192,7 +202,7 @@ struct Table {
         int m = pick2 ? m2 : m1;
         if (!rank_less(bs.scores[m], bs.keys[m], s, k))      // admission control
             return kRejected;
-        *victim = bs.keys[m];
+        take_victim(bs, m, victim);
         write_entry(bs, m, k, s, v);
         return kEvicted;
     }
@@ -218,8 +228,13 @@ struct Table {
         return false;
     }
 
+    // update_resident = false gives find_or_insert's insertion step: resident
+    // keys are left as they are.  evicted_out, when given, receives every
+    // entry that was resident before the call and is displaced by it
+    // (insert_and_evict), as it was when displaced.
     Counts insert_or_assign(uint64_t n, const uint64_t* keys, const float* values,
-                            const uint64_t* scores) {
+                            const uint64_t* scores, bool update_resident = true,
+                            std::vector<Victim>* evicted_out = nullptr) {
         Counts c;
         uint64_t step_score = step;
         std::vector<uint64_t> idx = last_occurrences(n, keys, c);
@@ -230,8 +245,10 @@ struct Table {
             uint64_t s = scores ? scores[i] : step_score;
             uint64_t b; int p;
             if (locate(k, &b, &p)) {              // HKV Algorithm 2, found branch
-                write_entry(at(b), p, k, s, values + i * dim);
-                ++c.updated;
+                if (update_resident) {
+                    write_entry(at(b), p, k, s, values + i * dim);
+                    ++c.updated;
+                }
             } else {
                 absent.push_back(i);
             }
@@ -244,13 +261,16 @@ struct Table {
         for (uint64_t i : absent) {
             uint64_t k = keys[i];
             uint64_t s = scores ? scores[i] : step_score;
-            uint64_t victim = 0;
+            Victim victim;
             Outcome o = dual ? insert_dual(k, s, values + i * dim, &victim)
                              : insert_single(bucket1(k), k, s, values + i * dim, &victim);
             if (o == kRejected) continue;
             admitted.insert(k);
             if (o == kEvicted) {
-                if (admitted.erase(victim) == 0) ++c.evicted;
+                if (admitted.erase(victim.key) == 0) {
+                    ++c.evicted;
+                    if (evicted_out) evicted_out->push_back(std::move(victim));
+                }
             }
         }
         c.admitted = admitted.size();
@@ -380,6 +400,46 @@ void oracle_assign(void* h, uint64_t n, const uint64_t* keys, const float* value
 
 void oracle_erase(void* h, uint64_t n, const uint64_t* keys, oracle_counts* out) {
     put(static_cast<Table*>(h)->erase(n, keys), out);
+}
+
+// insert_and_evict (HKV §4.1): insert_or_assign that also returns the entries
+// resident before the call that it displaced, sorted by key.  Outputs need
+// room for n entries; *count_out receives their number.
+void oracle_insert_and_evict(void* h, uint64_t n, const uint64_t* keys, const float* values,
+                             const uint64_t* scores, uint64_t* ev_keys, float* ev_values,
+                             uint64_t* ev_scores, uint64_t* count_out, oracle_counts* out) {
+    Table* t = static_cast<Table*>(h);
+    std::vector<Table::Victim> ev;
+    put(t->insert_or_assign(n, keys, values, scores, true, &ev), out);
+    std::sort(ev.begin(), ev.end(),
+              [](const Table::Victim& a, const Table::Victim& b) { return a.key < b.key; });
+    for (size_t i = 0; i < ev.size(); ++i) {
+        ev_keys[i] = ev[i].key;
+        ev_scores[i] = ev[i].score;
+        std::memcpy(ev_values + i * t->dim, ev[i].value.data(), sizeof(float) * t->dim);
+    }
+    *count_out = ev.size();
+}
+
+// find_or_insert (HKV §4.1): absent keys are inserted with their row of
+// values_inout (and their score) under Algorithm 2; resident keys are left
+// as they are.  Then every key that is resident after the call gets
+// found_out = 1 and its stored row in values_inout; the others get
+// found_out = 0 and keep their row.
+void oracle_find_or_insert(void* h, uint64_t n, const uint64_t* keys, float* values_inout,
+                           const uint64_t* scores, uint8_t* found_out, oracle_counts* out) {
+    Table* t = static_cast<Table*>(h);
+    put(t->insert_or_assign(n, keys, values_inout, scores, false, nullptr), out);
+    t->find(n, keys, values_inout, found_out, nullptr);
+}
+
+// contains (HKV §3.5 reader): found_out[i] = 1 iff keys[i] is resident.
+void oracle_contains(void* h, uint64_t n, const uint64_t* keys, uint8_t* found_out) {
+    Table* t = static_cast<Table*>(h);
+    for (uint64_t i = 0; i < n; ++i) {
+        uint64_t b; int p;
+        found_out[i] = (!is_reserved(keys[i]) && t->locate(keys[i], &b, &p)) ? 1 : 0;
+    }
 }
 
 uint64_t oracle_find(void* h, uint64_t n, const uint64_t* keys, float* values_out,

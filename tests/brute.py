@@ -71,7 +71,10 @@ class BruteTable:
         return {k for b in self.bk.values() for k in b}
 
     # -- operations --------------------------------------------------------
-    def insert_or_assign(self, keys, values, scores=None):
+    def insert_or_assign(self, keys, values, scores=None, update_resident=True, evicted_out=None):
+        """update_resident=False: find_or_insert's insertion step (resident
+        keys untouched).  evicted_out: list receiving (key, score, values) of
+        the entries resident before the call and displaced by it."""
         keys = [int(k) for k in keys]
         values = np.asarray(values, np.float32).reshape(len(keys), self.dim)
         order, reserved = self._last(keys)
@@ -83,10 +86,12 @@ class BruteTable:
             k = keys[i]
             b = self.where(k)
             if b is not None:
-                self.bk[b][k] = (s_of(i), tuple(values[i].tolist()))
-                updated += 1
+                if update_resident:
+                    self.bk[b][k] = (s_of(i), tuple(values[i].tolist()))
+                    updated += 1
             else:
                 absent.append(i)
+        snapshot = {k: sv for d in self.bk.values() for k, sv in d.items()}
         if self.dual:
             for i in absent:
                 self._dual_insert(keys[i], s_of(i), tuple(values[i].tolist()))
@@ -99,6 +104,8 @@ class BruteTable:
                     top = sorted(d.items(), key=lambda kv: (kv[1][0], kv[0]), reverse=True)[:SLOTS]
                     self.bk[b] = dict(top)
         after = self.residents()
+        if evicted_out is not None:
+            evicted_out.extend((k, snapshot[k][0], snapshot[k][1]) for k in sorted(before - after))
         absent_keys = {keys[i] for i in absent}
         if scores is None:
             self.step += 1
@@ -144,6 +151,13 @@ class BruteTable:
             b = self.where(k)
             if b is not None:
                 del self.bk[b][k]
+
+    def find_or_insert(self, keys, values, scores=None):
+        c = self.insert_or_assign(keys, values, scores, update_resident=False)
+        vals = np.asarray(values, np.float32).reshape(len(keys), self.dim).copy()
+        fv, found, _ = self.find(keys)
+        vals[found.astype(bool)] = fv[found.astype(bool)]
+        return c, vals, found
 
     def find(self, keys):
         n = len(keys)

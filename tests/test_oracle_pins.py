@@ -363,3 +363,48 @@ def test_find_is_membership(oracle_mod):
             assert found[i] == 1 and scs[i] == rs[j] and np.array_equal(vals[i], rv[j])
         else:
             assert found[i] == 0
+
+
+# --------------------------------------------------------------------------
+# The cache-workflow operations of HKV §4.1 (insert_and_evict,
+# find_or_insert) and §3.5 (contains), against the brute-force model.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("num_buckets,dim", [(1, 2), (3, 3), (7, 4)])
+def test_cache_workflow_ops_vs_brute(oracle_mod, seed, num_buckets, dim):
+    rng = np.random.default_rng(100 + seed)
+    t = oracle_mod.OracleTable(num_buckets, dim)
+    ref = BruteTable(num_buckets, dim)
+    universe = wl.unique_keys(seed + 2000, 3 * 128 * num_buckets)
+    for _ in range(25):
+        op = rng.choice(["iae", "fio", "ioa", "contains", "erase"])
+        n = int(rng.integers(0, 2 * 128 * num_buckets))
+        keys = universe[rng.integers(0, universe.size, n)]
+        vals = rng.standard_normal((n, dim)).astype(np.float32)
+        scores = rng.integers(0, 40, n).astype(np.uint64)
+        use_s = rng.random() < 0.7
+        s = scores if use_s else None
+        if op == "iae":
+            c, (ek, ev, es) = t.insert_and_evict(keys, vals, s)
+            out = []
+            r = ref.insert_or_assign(keys, vals, s, evicted_out=out)
+            assert ek.tolist() == [x[0] for x in out]
+            assert es.tolist() == [x[1] for x in out]
+            assert np.array_equal(ev, np.array([x[2] for x in out], np.float32).reshape(len(out), dim))
+            assert c["evicted"] == r["evicted"] == len(out)
+        elif op == "fio":
+            c, v, f = t.find_or_insert(keys, vals, s)
+            rc, rv, rf = ref.find_or_insert(keys, vals, s)
+            assert np.array_equal(f, rf) and np.array_equal(v, rv)
+            assert c["updated"] == 0
+            for fld in ("admitted", "rejected", "evicted"):
+                assert c[fld] == rc[fld]
+        elif op == "ioa":
+            t.insert_or_assign(keys, vals, s)
+            ref.insert_or_assign(keys, vals, s)
+        elif op == "contains":
+            assert np.array_equal(t.contains(keys), ref.find(keys)[1])
+        else:
+            t.erase(keys)
+            ref.erase(keys)
+        _compare(t, ref)
