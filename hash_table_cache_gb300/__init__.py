@@ -43,6 +43,7 @@ EXPORTS = (
     "hkv_create", "hkv_destroy", "hkv_find", "hkv_insert_or_assign", "hkv_assign", "hkv_erase",
     "hkv_size", "hkv_export", "hkv_get_error_counts", "hkv_get_op_counts",
     "hkv_reset_op_counts", "hkv_get_info", "hkv_status_string", "hkv_insert_or_assign_noalloc",
+    "hkv_insert_and_evict", "hkv_find_or_insert", "hkv_contains", "hkv_find_ptr",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -91,6 +92,10 @@ def load(path: str = LIB_PATH):
         "hkv_insert_or_assign": [vp, u64, vp, vp, vp, vp],
         "hkv_insert_or_assign_noalloc": [vp, u64, vp, vp, vp, vp],
         "hkv_assign": [vp, u64, vp, vp, vp, vp],
+        "hkv_insert_and_evict": [vp, u64, vp, vp, vp, vp, vp, vp, vp, vp],
+        "hkv_find_or_insert": [vp, u64, vp, vp, vp, vp, vp],
+        "hkv_contains": [vp, u64, vp, vp, vp],
+        "hkv_find_ptr": [vp, u64, vp, vp, vp, vp, vp],
         "hkv_erase": [vp, u64, vp, vp],
         "hkv_size": [vp, ctypes.POINTER(u64), vp],
         "hkv_export": [vp, u64, u64, u64, vp, vp, vp, vp, vp],
@@ -156,6 +161,26 @@ def hkv_insert_or_assign_noalloc(table, n, keys, values, scores=None, stream=Non
     limit, the sharing rule and the first-call set-up)."""
     return load().hkv_insert_or_assign_noalloc(table, int(n), _p(keys), _p(values), _p(scores),
                                                _s(stream))
+
+
+def hkv_insert_and_evict(table, n, keys, values, scores, ev_keys, ev_values, ev_scores, ev_count,
+                         stream=None):
+    return load().hkv_insert_and_evict(table, int(n), _p(keys), _p(values), _p(scores), _p(ev_keys),
+                                       _p(ev_values), _p(ev_scores), _p(ev_count), _s(stream))
+
+
+def hkv_find_or_insert(table, n, keys, values_inout, scores, found_out, stream=None):
+    return load().hkv_find_or_insert(table, int(n), _p(keys), _p(values_inout), _p(scores),
+                                     _p(found_out), _s(stream))
+
+
+def hkv_contains(table, n, keys, found_out, stream=None):
+    return load().hkv_contains(table, int(n), _p(keys), _p(found_out), _s(stream))
+
+
+def hkv_find_ptr(table, n, keys, ptrs_out, found_out, scores_out=None, stream=None):
+    return load().hkv_find_ptr(table, int(n), _p(keys), _p(ptrs_out), _p(found_out),
+                               _p(scores_out), _s(stream))
 
 
 def hkv_assign(table, n, keys, values, scores=None, stream=None):
@@ -265,6 +290,44 @@ class HashTable:
     def insert_or_assign(self, keys, values, scores=None, stream=None):
         _check(hkv_insert_or_assign(self.handle, keys.numel(), keys, values, scores, stream),
                "hkv_insert_or_assign")
+
+    def insert_and_evict(self, keys, values, scores=None, stream=None):
+        """Returns (evicted keys, values, scores) -- unsorted, on the device."""
+        import torch
+        n = keys.numel()
+        dev = keys.device
+        ek = torch.empty(max(n, 1), dtype=torch.int64, device=dev)
+        ev = torch.empty((max(n, 1), self.dim), dtype=torch.float32, device=dev)
+        es = torch.empty(max(n, 1), dtype=torch.int64, device=dev)
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        _check(hkv_insert_and_evict(self.handle, n, keys, values, scores, ek, ev, es, cnt, stream),
+               "hkv_insert_and_evict")
+        c = int(cnt.item())
+        return ek[:c], ev[:c], es[:c]
+
+    def find_or_insert(self, keys, values_inout, scores=None, stream=None):
+        """values_inout is updated in place; returns the found flags."""
+        import torch
+        found = torch.empty(keys.numel(), dtype=torch.uint8, device=keys.device)
+        _check(hkv_find_or_insert(self.handle, keys.numel(), keys, values_inout, scores, found,
+                                  stream), "hkv_find_or_insert")
+        return found
+
+    def contains(self, keys, stream=None):
+        import torch
+        found = torch.empty(keys.numel(), dtype=torch.uint8, device=keys.device)
+        _check(hkv_contains(self.handle, keys.numel(), keys, found, stream), "hkv_contains")
+        return found
+
+    def find_ptr(self, keys, with_scores=True, stream=None):
+        """Returns (row addresses as int64, found, scores)."""
+        import torch
+        n = keys.numel()
+        ptrs = torch.empty(n, dtype=torch.int64, device=keys.device)
+        found = torch.empty(n, dtype=torch.uint8, device=keys.device)
+        scs = torch.empty(n, dtype=torch.int64, device=keys.device) if with_scores else None
+        _check(hkv_find_ptr(self.handle, n, keys, ptrs, found, scs, stream), "hkv_find_ptr")
+        return ptrs, found, scs
 
     def assign(self, keys, values, scores=None, stream=None):
         _check(hkv_assign(self.handle, keys.numel(), keys, values, scores, stream), "hkv_assign")

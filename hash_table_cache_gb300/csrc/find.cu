@@ -21,24 +21,16 @@ namespace {
 #ifndef HKV_FIND_MIN_BLOCKS
 #define HKV_FIND_MIN_BLOCKS 4
 #endif
-#ifndef HKV_FIND_SPECULATE
-#define HKV_FIND_SPECULATE 0
-#endif
-constexpr bool kFindSpeculate = HKV_FIND_SPECULATE != 0;
+
 constexpr int kFindKeysPerTile = HKV_FIND_KEYS_PER_TILE;
 
 // Probe for U keys at once: the U digest-line loads, then the U first-match
 // key loads, are issued back to back so a tile keeps U requests in flight.
-// With kSpec the tile also loads, together with the key confirm, the first
-// 16-byte chunk of each lane's share of the value row of the first digest
-// match (the true slot for ~3/4 of hits), which removes one dependent round
-// trip from most hits; `spec_slot` tells which slot that chunk belongs to.
-template <int U, bool kSpec>
+template <int U>
 __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64_t (&b)[U],
                                                 const uint64_t (&k)[U], const uint32_t (&pat)[U],
                                                 const bool (&act)[U], unsigned sub, unsigned tmask,
-                                                bool spec_ok, int (&slot)[U], int (&spec_slot)[U],
-                                                uint4 (&spec)[U]) {
+                                                int (&slot)[U]) {
   uint4 dg[U];
 #pragma unroll
   for (int u = 0; u < U; ++u)
@@ -50,17 +42,6 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
     if (act[u])
       m[u] = byte_match4(dg[u].x, pat[u]) | (byte_match4(dg[u].y, pat[u]) << 4) |
              (byte_match4(dg[u].z, pat[u]) << 8) | (byte_match4(dg[u].w, pat[u]) << 12);
-  }
-  if (kSpec) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const unsigned cb = __ballot_sync(tmask, m[u] != 0) & tmask;
-      const int src = cb ? __ffs(cb) - 1 : static_cast<int>(lane_id());
-      const int fb = __shfl_sync(tmask, m[u] ? __ffs(m[u]) - 1 : 0, src);
-      spec_slot[u] = cb ? static_cast<int>((src & 7) * 16 + fb) : -1;
-      if (spec_ok && spec_slot[u] >= 0)
-        spec[u] = ld_stream_v4(row_ptr(t, b[u] * kSlots + spec_slot[u]) + 4 * sub);
-    }
   }
   uint64_t kk[U];
 #pragma unroll
@@ -94,12 +75,15 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
   }
 }
 
+// What a find writes per key besides the found flag (and the score).
+enum FindOut { kOutValues = 0, kOutNone = 1, kOutPointer = 2 };
+
 // One 8-lane tile handles U keys per iteration: keys i, i+T, ..., i+(U-1)T
 // for T tiles in the grid.
-template <bool kDual, int U>
-__global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS) find_kernel(TableView t, uint64_t n, const uint64_t* keys,
-                                                   float* values_out, uint8_t* found_out,
-                                                   uint64_t* scores_out, bool vec) {
+template <bool kDual, int U, int kOut>
+__global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
+    find_kernel(TableView t, uint64_t n, const uint64_t* keys, float* values_out,
+                float** ptrs_out, uint8_t* found_out, uint64_t* scores_out, bool vec) {
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
@@ -124,49 +108,29 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS) find_kernel(TableVie
       pat[u] = digest_of_hash(h) * 0x01010101u;
       b[u] = bucket_of_hash(t, h);
     }
-    int slot[U], spec_slot[U];
-    uint4 spec[U];
-    // speculation covers one 16-byte chunk per lane: rows of at most 32 floats
-    const bool spec_ok = vec && t.dim <= 32 && sub < (t.dim >> 2);
-    tile_probe_many<U, kFindSpeculate>(t, b, k, pat, act, sub, tmask, spec_ok, slot, spec_slot,
-                                       spec);
+    int slot[U];
+    tile_probe_many<U>(t, b, k, pat, act, sub, tmask, slot);
     if (kDual) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (act[u] && slot[u] < 0) {
-          spec_slot[u] = -1;  // the speculative chunk belongs to the first bucket
           b[u] = bucket2_of(t, k[u], b[u]);
           slot[u] = tile_probe<true>(t, b[u], k[u], pat[u], sub, tmask);
         }
       }
     }
-    // Value rows: U loads in flight, then U streaming stores.
-    const float* src[U];
-    float* dst[U];
+    if (kOut == kOutValues) {
+      // Value rows: U loads in flight, then U streaming stores.
+      const float* src[U];
+      float* dst[U];
+      bool ok[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      src[u] = slot[u] >= 0 ? row_ptr(t, b[u] * kSlots + slot[u]) : nullptr;
-      dst[u] = values_out + (i0 + u * tiles) * t.dim;
-    }
-    if (vec) {
-      const uint32_t chunks = t.dim >> 2;
-      for (uint32_t c = sub; c < chunks; c += 8) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (!src[u]) continue;
-          if (kFindSpeculate && spec_ok && slot[u] == spec_slot[u]) v[u] = spec[u];
-          else v[u] = ld_stream_v4(src[u] + 4 * c);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (src[u]) st_stream_v4(dst[u] + 4 * c, v[u]);
+      for (int u = 0; u < U; ++u) {
+        ok[u] = slot[u] >= 0;
+        src[u] = ok[u] ? row_ptr(t, b[u] * kSlots + slot[u]) : nullptr;
+        dst[u] = values_out + (i0 + u * tiles) * t.dim;
       }
-    } else {
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (src[u])
-          for (uint32_t c = sub; c < t.dim; c += 8) dst[u][c] = src[u][c];
+      tile_copy_rows<U>(dst, src, ok, t.dim, sub, vec);
     }
     if (sub == 0) {
 #pragma unroll
@@ -174,26 +138,42 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS) find_kernel(TableVie
         const uint64_t i = i0 + u * tiles;
         if (i >= n) continue;
         found_out[i] = slot[u] >= 0 ? 1 : 0;
-        if (slot[u] >= 0 && scores_out) scores_out[i] = *score_at(t, b[u] * kSlots + slot[u]);
+        const uint64_t row = b[u] * kSlots + static_cast<uint64_t>(slot[u]);
+        if (kOut == kOutPointer) ptrs_out[i] = slot[u] >= 0 ? row_ptr(t, row) : nullptr;
+        if (slot[u] >= 0 && scores_out) scores_out[i] = *score_at(t, row);
       }
     }
   }
   if (reserved) atomicAdd(&t.stats->reserved, reserved);
 }
 
-template <bool kDual, int U>
+template <bool kDual, int U, int kOut>
 cudaError_t launch_find_u(const TableView& t, uint64_t n, const uint64_t* keys, float* values_out,
-                          uint8_t* found_out, uint64_t* scores_out, bool vec, cudaStream_t st) {
+                          float** ptrs_out, uint8_t* found_out, uint64_t* scores_out, bool vec,
+                          cudaStream_t st) {
   const int threads = 256;
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, find_kernel<kDual, U>, threads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, find_kernel<kDual, U, kOut>, threads, 0);
   if (per_sm < 1) per_sm = 1;
   uint64_t blocks = (n * 8 + threads * U - 1) / (threads * U);
   const uint64_t cap = static_cast<uint64_t>(sm_count()) * per_sm;
   if (blocks > cap) blocks = cap;
-  find_kernel<kDual, U><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      t, n, keys, values_out, found_out, scores_out, vec);
+  find_kernel<kDual, U, kOut><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      t, n, keys, values_out, ptrs_out, found_out, scores_out, vec);
   return cudaGetLastError();
+}
+
+template <int kOut>
+cudaError_t launch_find_mode(const TableView& t, uint64_t n, const uint64_t* keys,
+                             float* values_out, float** ptrs_out, uint8_t* found_out,
+                             uint64_t* scores_out, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values_out) & 15) == 0);
+  if (t.dual)
+    return launch_find_u<true, kFindKeysPerTile, kOut>(t, n, keys, values_out, ptrs_out,
+                                                        found_out, scores_out, vec, st);
+  return launch_find_u<false, kFindKeysPerTile, kOut>(t, n, keys, values_out, ptrs_out, found_out,
+                                                       scores_out, vec, st);
 }
 
 }  // namespace
@@ -213,12 +193,17 @@ int sm_count() {
 
 cudaError_t launch_find(const TableView& t, uint64_t n, const uint64_t* keys, float* values_out,
                         uint8_t* found_out, uint64_t* scores_out, cudaStream_t st) {
-  if (n == 0) return cudaSuccess;
-  const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values_out) & 15) == 0);
-  if (t.dual) return launch_find_u<true, kFindKeysPerTile>(t, n, keys, values_out, found_out,
-                                                           scores_out, vec, st);
-  return launch_find_u<false, kFindKeysPerTile>(t, n, keys, values_out, found_out, scores_out,
-                                                vec, st);
+  return launch_find_mode<kOutValues>(t, n, keys, values_out, nullptr, found_out, scores_out, st);
+}
+
+cudaError_t launch_contains(const TableView& t, uint64_t n, const uint64_t* keys,
+                            uint8_t* found_out, cudaStream_t st) {
+  return launch_find_mode<kOutNone>(t, n, keys, nullptr, nullptr, found_out, nullptr, st);
+}
+
+cudaError_t launch_find_ptr(const TableView& t, uint64_t n, const uint64_t* keys, float** ptrs_out,
+                            uint8_t* found_out, uint64_t* scores_out, cudaStream_t st) {
+  return launch_find_mode<kOutPointer>(t, n, keys, nullptr, ptrs_out, found_out, scores_out, st);
 }
 
 }  // namespace hkv

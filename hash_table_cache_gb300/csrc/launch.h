@@ -37,9 +37,25 @@ cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, S
 cudaError_t launch_find(const TableView& t, uint64_t n, const uint64_t* keys, float* values_out,
                         uint8_t* found_out, uint64_t* scores_out, cudaStream_t st);
 
+cudaError_t launch_contains(const TableView& t, uint64_t n, const uint64_t* keys,
+                            uint8_t* found_out, cudaStream_t st);
+
+cudaError_t launch_find_ptr(const TableView& t, uint64_t n, const uint64_t* keys, float** ptrs_out,
+                            uint8_t* found_out, uint64_t* scores_out, cudaStream_t st);
+
+// Variants of the single-mode upsert: find_or_insert leaves resident keys
+// untouched; insert_and_evict reports the pre-call residents it displaces.
+struct UpsertExtra {
+  bool update_resident = true;
+  uint64_t* ev_keys = nullptr;
+  float* ev_values = nullptr;
+  uint64_t* ev_scores = nullptr;
+  unsigned long long* ev_count = nullptr;
+};
+
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
                           const uint64_t* keys, const float* values, const uint64_t* scores,
-                          uint64_t step_score, cudaStream_t st);
+                          uint64_t step_score, cudaStream_t st, const UpsertExtra& ex = UpsertExtra());
 
 cudaError_t launch_assign(const TableView& t, const UpsertScratch& s, uint64_t n,
                           const uint64_t* keys, const float* values, const uint64_t* scores,

@@ -328,6 +328,81 @@ hkv_status hkv_insert_or_assign(hkv_table* t, uint64_t n, const uint64_t* keys, 
   });
 }
 
+hkv_status hkv_contains(hkv_table* t, uint64_t n, const uint64_t* keys, uint8_t* found_out,
+                        void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !found_out)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kReader, stream, [&](cudaStream_t s) {
+    return from_cuda(hkv::launch_contains(t->v, n, keys, found_out, s));
+  });
+}
+
+hkv_status hkv_find_ptr(hkv_table* t, uint64_t n, const uint64_t* keys, float** values_ptr_out,
+                        uint8_t* found_out, uint64_t* scores_out, void* stream) {
+  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (n && (!keys || !values_ptr_out || !found_out)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kReader, stream, [&](cudaStream_t s) {
+    return from_cuda(hkv::launch_find_ptr(t->v, n, keys, values_ptr_out, found_out, scores_out, s));
+  });
+}
+
+namespace {
+
+// Single-mode upsert variant with its own scratch (insert_and_evict,
+// find_or_insert).
+hkv_status upsert_variant(hkv_table* t, cudaStream_t s, uint64_t n, const uint64_t* keys,
+                          const float* values, const uint64_t* scores,
+                          const hkv::UpsertExtra& ex) {
+  const uint64_t step_score = t->step;
+  if (!scores) ++t->step;
+  if (n == 0) return HKV_OK;
+  void* mem = nullptr;
+  hkv_status st = scratch_call(t, s, n, hkv::ScratchKind::kSingleUpsert, &mem);
+  if (st != HKV_OK) return st;
+  hkv::UpsertScratch sc =
+      hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, hkv::ScratchKind::kSingleUpsert);
+  cudaError_t e =
+      hkv::clear_upsert_scratch(sc, t->v.num_buckets, hkv::ScratchKind::kSingleUpsert, s);
+  if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, scores, step_score, s, ex);
+  cudaError_t f = cudaFreeAsync(mem, s);
+  return from_cuda(e != cudaSuccess ? e : f);
+}
+
+}  // namespace
+
+hkv_status hkv_insert_and_evict(hkv_table* t, uint64_t n, const uint64_t* keys,
+                                const float* values, const uint64_t* scores,
+                                uint64_t* evicted_keys_out, float* evicted_values_out,
+                                uint64_t* evicted_scores_out, uint64_t* evicted_count_out,
+                                void* stream) {
+  if (!batch_ok(t, n) || t->v.dual) return HKV_ERR_INVALID;
+  if (n && (!keys || !values)) return HKV_ERR_INVALID;
+  if (!evicted_keys_out || !evicted_count_out) return HKV_ERR_INVALID;
+  return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
+    cudaError_t e = cudaMemsetAsync(evicted_count_out, 0, sizeof(uint64_t), s);
+    if (e != cudaSuccess) return from_cuda(e);
+    hkv::UpsertExtra ex;
+    ex.ev_keys = evicted_keys_out;
+    ex.ev_values = evicted_values_out;
+    ex.ev_scores = evicted_scores_out;
+    ex.ev_count = reinterpret_cast<unsigned long long*>(evicted_count_out);
+    return upsert_variant(t, s, n, keys, values, scores, ex);
+  });
+}
+
+hkv_status hkv_find_or_insert(hkv_table* t, uint64_t n, const uint64_t* keys, float* values_inout,
+                              const uint64_t* scores, uint8_t* found_out, void* stream) {
+  if (!batch_ok(t, n) || t->v.dual) return HKV_ERR_INVALID;
+  if (n && (!keys || !values_inout || !found_out)) return HKV_ERR_INVALID;
+  return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
+    hkv::UpsertExtra ex;
+    ex.update_resident = false;
+    hkv_status st = upsert_variant(t, s, n, keys, values_inout, scores, ex);
+    if (st != HKV_OK) return st;
+    return from_cuda(hkv::launch_find(t->v, n, keys, values_inout, found_out, nullptr, s));
+  });
+}
+
 hkv_status hkv_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
                       const uint64_t* scores, void* stream) {
   if (!batch_ok(t, n)) return HKV_ERR_INVALID;

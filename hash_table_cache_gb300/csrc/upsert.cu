@@ -224,7 +224,7 @@ __device__ __forceinline__ uint64_t warp_min_u64(uint64_t v, bool valid, unsigne
 
 __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
-    const uint64_t* scores_in, uint64_t step_score, bool vec) {
+    const uint64_t* scores_in, uint64_t step_score, bool vec, UpsertExtra ex) {
   (void)keys_in;  // entry keys come from the stage
   __shared__ BucketStage stage_all[kThreads / 32];
   const unsigned lane = lane_id();
@@ -313,13 +313,13 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
             }
           }
         }
-        if (hs >= 0) {
+        if (hs >= 0 && ex.update_resident) {
           st.occ[hs] = e;
           st.score[hs] = scores_in ? scores_in[e] : step_score;
         }
       }
       const unsigned hm = __ballot_sync(0xFFFFFFFFu, hs >= 0);
-      if (lane == 0) n_upd += __popc(hm);
+      if (lane == 0 && ex.update_resident) n_upd += __popc(hm);
       return hs >= 0;
     };
 
@@ -424,8 +424,23 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         if (q < head) {
           const uint32_t slot = rq[q];
           st.list[pos++] = static_cast<uint8_t>(slot);
-          if (st.fresh[slot >> 5] & (1u << (slot & 31))) ++fr;  // admitted earlier this call
-          else ++ev;                                             // pre-call resident
+          if (st.fresh[slot >> 5] & (1u << (slot & 31))) {
+            ++fr;  // admitted earlier this call
+          } else {
+            ++ev;  // pre-call resident
+            if (ex.ev_keys) {  // insert_and_evict: report it as it is now
+              const unsigned long long o = atomicAdd(ex.ev_count, 1ull);
+              ex.ev_keys[o] = st.key[slot];
+              if (ex.ev_scores) ex.ev_scores[o] = st.score[slot];
+              if (ex.ev_values) {
+                const uint32_t src_i = st.occ[slot];  // updated by this call: its input row
+                const float* src = src_i != kNone ? values_in + static_cast<uint64_t>(src_i) * t.dim
+                                                  : row_ptr(t, b * kSlots + slot);
+                float* dst = ex.ev_values + o * t.dim;
+                for (uint32_t c = 0; c < t.dim; ++c) dst[c] = src[c];
+              }
+            }
+          }
         }
       }
       const uint32_t n_ev = __reduce_add_sync(0xFFFFFFFFu, ev);
@@ -932,14 +947,14 @@ cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, S
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
                           const uint64_t* keys, const float* values, const uint64_t* scores,
-                          uint64_t step_score, cudaStream_t st) {
+                          uint64_t step_score, cudaStream_t st, const UpsertExtra& ex) {
   if (n == 0) return cudaSuccess;
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
   if (!t.dual) {
     stage_kernel<<<grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread), kThreads, 0,
                    st>>>(t, s, n, keys);
     upsert_single_kernel<<<grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS), kThreads, 0, st>>>(
-        t, s, keys, values, scores, step_score, vec);
+        t, s, keys, values, scores, step_score, vec, ex);
   } else {
     dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, t.stats);
     dual_resident_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, scores,

@@ -114,7 +114,46 @@ hkv_status hkv_find(hkv_table* table, uint64_t n, const uint64_t* keys, float* v
 hkv_status hkv_insert_or_assign(hkv_table* table, uint64_t n, const uint64_t* keys,
                                 const float* values, const uint64_t* scores, void* stream);
 
-/* Updater.  HKV §3.5: overwrites the value (and the score when scores !=
+/* Inserter, single-bucket tables only (HKV §7: the dual-bucket mode covers
+ * insert_or_assign and find).  HKV §4.1 insert_and_evict: the same update as
+ * hkv_insert_or_assign, and every entry that was resident before the call
+ * and is displaced by it is written to evicted_keys_out / evicted_values_out
+ * / evicted_scores_out (values and scores may be NULL) as it was when
+ * displaced (a key updated by this call and then displaced carries its new
+ * value and score), at consecutive positions in unspecified order;
+ * *evicted_count_out (device) receives their number.  Outputs need room for
+ * n entries.  Dual-mode tables return HKV_ERR_INVALID. */
+hkv_status hkv_insert_and_evict(hkv_table* table, uint64_t n, const uint64_t* keys,
+                                const float* values, const uint64_t* scores,
+                                uint64_t* evicted_keys_out, float* evicted_values_out,
+                                uint64_t* evicted_scores_out, uint64_t* evicted_count_out,
+                                void* stream);
+
+/* Inserter, single-bucket tables only.  HKV §4.1 find_or_insert (lookup
+ * with insertion for cold start): absent keys are inserted with their row of
+ * values_inout and their score (scores, or the step counter when NULL) under
+ * HKV Algorithm 2; resident keys are not modified.  Afterwards, for each i:
+ * when keys[i] is resident, found_out[i] = 1 and row i of values_inout holds
+ * its stored value; otherwise (admission rejected it) found_out[i] = 0 and
+ * row i is left unchanged.  Dual-mode tables return HKV_ERR_INVALID. */
+hkv_status hkv_find_or_insert(hkv_table* table, uint64_t n, const uint64_t* keys,
+                              float* values_inout, const uint64_t* scores, uint8_t* found_out,
+                              void* stream);
+
+/* Reader.  HKV §3.5 contains: found_out[i] = 1 iff keys[i] is resident.
+ * Reads digests and keys only, no value row. */
+hkv_status hkv_contains(hkv_table* table, uint64_t n, const uint64_t* keys, uint8_t* found_out,
+                        void* stream);
+
+/* Reader.  HKV §5.2-§5.3 find*: like hkv_find, but instead of copying a
+ * resident key's value row, values_ptr_out[i] receives the device address of
+ * the row inside the table (HBM, or the mapped host slab in tiered mode);
+ * NULL on a miss.  The addresses stay valid until the next inserter call on
+ * the table (insert_or_assign, insert_and_evict, find_or_insert, erase). */
+hkv_status hkv_find_ptr(hkv_table* table, uint64_t n, const uint64_t* keys, float** values_ptr_out,
+                        uint8_t* found_out, uint64_t* scores_out, void* stream);
+
+/* Updater.  HKV §3.5: overwrites the value/* Updater.  HKV §3.5: overwrites the value (and the score when scores !=
  * NULL) of resident keys in place; absent keys are ignored; nothing is
  * inserted, evicted or moved. */
 hkv_status hkv_assign(hkv_table* table, uint64_t n, const uint64_t* keys, const float* values,

@@ -54,3 +54,15 @@ def find_compare(t, o, q):
     assert np.array_equal(gv.cpu().numpy().view(np.uint32), ov.view(np.uint32)), "values differ"
     assert np.array_equal(u64(gs), os_), "scores differ"
     return int(of.sum())
+
+
+def read_device(addr, nbytes):
+    """Copy nbytes at a raw device address to a numpy byte array (CUDA runtime
+    already loaded by torch)."""
+    import ctypes
+    rt = ctypes.CDLL("libcudart.so.13")
+    buf = np.empty(nbytes, np.uint8)
+    err = rt.cudaMemcpy(ctypes.c_void_p(buf.ctypes.data), ctypes.c_void_p(int(addr)),
+                        ctypes.c_size_t(nbytes), ctypes.c_int(2))
+    assert err == 0, err
+    return buf
