@@ -190,6 +190,8 @@ struct BucketStage {
   uint32_t occ[kSlots];
   uint32_t dig[kSlots / 4];
   uint32_t fresh[kSlots / 32];
+  uint32_t dhead[256];   // digest -> first slot carrying it (0xFF: none)
+  uint8_t dnext[kSlots];  // next slot with the same digest (0xFF: end)
   uint8_t list[kSlots];  // free-slot list, later the dirty-slot list
 };
 
@@ -270,6 +272,15 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     *reinterpret_cast<ulonglong2*>(&st.score[lane * 4 + 2]) = make_ulonglong2(kv[2].y, kv[3].y);
     *reinterpret_cast<uint4*>(&st.occ[lane * 4]) = make_uint4(kNone, kNone, kNone, kNone);
     st.dig[lane] = dw;
+    // Reverse digest index of the bucket: a chain of slots per digest value.
+    reinterpret_cast<uint4*>(st.dhead)[2 * lane] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
+    reinterpret_cast<uint4*>(st.dhead)[2 * lane + 1] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t d = (dw >> (8 * q)) & 0xFFu;
+      if (d) st.dnext[lane * 4 + q] = static_cast<uint8_t>(atomicExch(&st.dhead[d], lane * 4 + q));
+    }
     if (lane < 4) st.fresh[lane] = 0;
 
     // Entry of chunk c for this lane: batch index if the stage position holds
@@ -298,20 +309,15 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     auto phase_a = [&](uint32_t e, uint64_t ke) -> bool {
       int hs = -1;
       if (e != kNone) {
-        const uint32_t pat = digest_of_hash(hash64(ke)) * 0x01010101u;
-#pragma unroll 1
-        for (int w4 = 0; w4 < kSlots / 16 && hs < 0; ++w4) {
-          const uint4 d4 = reinterpret_cast<const uint4*>(st.dig)[w4];
-          uint32_t m = byte_match4(d4.x, pat) | (byte_match4(d4.y, pat) << 4) |
-                       (byte_match4(d4.z, pat) << 8) | (byte_match4(d4.w, pat) << 12);
-          while (m) {
-            const int slot = w4 * 16 + __ffs(m) - 1;
-            m &= m - 1;
-            if (st.key[slot] == ke) {
-              hs = slot;
-              break;
-            }
+        // walk the slots whose digest equals the key's (HKV Algorithm 1's
+        // digest filter, through the bucket's reverse index)
+        uint32_t sl = st.dhead[digest_of_hash(hash64(ke))];
+        for (int guard = 0; sl != 0xFFu && guard < kSlots; ++guard) {
+          if (st.key[sl] == ke) {
+            hs = static_cast<int>(sl);
+            break;
           }
+          sl = st.dnext[sl];
         }
         if (hs >= 0 && ex.update_resident) {
           st.occ[hs] = e;
@@ -343,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         st.key[slot] = ke;
         st.score[slot] = se;
         st.occ[slot] = e;
+        reinterpret_cast<uint8_t*>(st.dig)[slot] = static_cast<uint8_t>(digest_of_hash(hash64(ke)));
         atomicOr(&st.fresh[slot >> 5], 1u << (slot & 31));
       }
       const uint32_t placed = min(static_cast<uint32_t>(__popc(mm)), nfree - used);
@@ -458,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         st.key[slot] = ke;
         st.score[slot] = se;
         st.occ[slot] = e;
+        reinterpret_cast<uint8_t*>(st.dig)[slot] = static_cast<uint8_t>(digest_of_hash(hash64(ke)));
         atomicOr(&st.fresh[slot >> 5], 1u << (slot & 31));
       }
       if (lane == 0) n_adm += __popc(am);
@@ -490,24 +498,21 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         ne += __popc(m);
       }
       __syncwarp();
-      bool hit[kWin];
-#pragma unroll
-      for (int c = 0; c < kWin; ++c) {
-        hit[c] = false;
-        if (32u * c < ne) {
-          const bool v = 32u * c + lane < ne;
-          hit[c] = phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey);
-        }
+      // (loops kept rolled: one copy of each phase keeps the code in cache)
+      uint32_t hits = 0;  // bit c: this lane's entry of dense chunk c hit
+#pragma unroll 1
+      for (uint32_t c = 0; 32u * c < ne; ++c) {
+        const bool v = 32u * c + lane < ne;
+        if (phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey))
+          hits |= 1u << c;
       }
       __syncwarp();
       build_free_list();
-#pragma unroll
-      for (int c = 0; c < kWin; ++c) {
-        if (32u * c < ne) {
-          const bool v = 32u * c + lane < ne;
-          const uint32_t e = v ? st.eidx[32 * c + lane] : kNone;
-          phase_b(e, v ? st.ekey[32 * c + lane] : kEmptyKey, v && !hit[c]);
-        }
+#pragma unroll 1
+      for (uint32_t c = 0; 32u * c < ne; ++c) {
+        const bool v = 32u * c + lane < ne;
+        const uint32_t e = v ? st.eidx[32 * c + lane] : kNone;
+        phase_b(e, v ? st.ekey[32 * c + lane] : kEmptyKey, v && !((hits >> c) & 1u));
       }
     } else {
       // Long run: walk it chunk by chunk from the stage, marking hits there.
@@ -541,16 +546,14 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     for (int q = 0; q < 4; ++q)
       if (st.occ[lane * 4 + q] != kNone) dm |= 1u << q;
     if (dm) {
-      uint32_t nd = dw;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         if (!(dm & (1u << q))) continue;
-        const uint64_t k = st.key[lane * 4 + q];
         *reinterpret_cast<ulonglong2*>(key_at(t, base + q)) =
-            make_ulonglong2(k, st.score[lane * 4 + q]);
-        nd = (nd & ~(0xFFu << (8 * q))) | (digest_of_hash(hash64(k)) << (8 * q));
+            make_ulonglong2(st.key[lane * 4 + q], st.score[lane * 4 + q]);
       }
-      *reinterpret_cast<uint32_t*>(t.digests + base) = nd;
+      const uint32_t nd = st.dig[lane];
+      if (nd != dw) *reinterpret_cast<uint32_t*>(t.digests + base) = nd;
     }
     uint32_t total;
     uint32_t pos = prefix_small(__popc(dm), total);
