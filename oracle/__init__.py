@@ -31,6 +31,9 @@ _LIB = os.path.join(_HERE, "libhkv_oracle.so")
 RESERVED_LO = 0xFFFFFFFFFFFFFFF0
 SLOTS = 128
 
+# Score policies (reading R10 in hkv_oracle.cpp; HKV §3.3, Table 8 names).
+POLICY_CUSTOMIZED, POLICY_LRU, POLICY_LFU, POLICY_EPOCH_LRU, POLICY_EPOCH_LFU = range(5)
+
 
 class _Counts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
@@ -61,7 +64,8 @@ def _load():
     lib = ctypes.CDLL(build())
     u64, u32, vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p
     sig = {
-        "oracle_create": (vp, [u64, u32, ctypes.c_int]),
+        "oracle_create": (vp, [u64, u32, ctypes.c_int, u32]),
+        "oracle_set_epoch": (None, [vp, u32]),
         "oracle_destroy": (None, [vp]),
         "oracle_set_bucket_filter": (ctypes.c_int, [vp, u64, vp]),
         "oracle_hash": (u64, [u64]),
@@ -101,16 +105,29 @@ def hash64(key: int) -> int:
 
 
 class OracleTable:
-    """Single-threaded model of one table (single or dual-bucket mode)."""
+    """Single-threaded model of one table (single or dual-bucket mode) under
+    one score policy (POLICY_*)."""
 
-    def __init__(self, num_buckets: int, dim: int, dual: bool = False):
+    def __init__(self, num_buckets: int, dim: int, dual: bool = False,
+                 policy: int = POLICY_CUSTOMIZED):
         lib = _load()
         self.num_buckets = int(num_buckets)
         self.dim = int(dim)
         self.dual = bool(dual)
-        self._h = lib.oracle_create(self.num_buckets, self.dim, int(self.dual))
+        self.policy = int(policy)
+        self._h = lib.oracle_create(self.num_buckets, self.dim, int(self.dual), self.policy)
         if not self._h:
             raise ValueError("oracle_create rejected the arguments")
+
+    def set_epoch(self, epoch: int):
+        _load().oracle_set_epoch(self._h, int(epoch) & 0xFFFFFFFF)
+
+    def _scores(self, scores):
+        if scores is None:
+            return None
+        if self.policy in (POLICY_LRU, POLICY_EPOCH_LRU):
+            raise ValueError("clock-driven policies take no caller scores")
+        return _keys(scores)
 
     def close(self):
         if self._h:
@@ -154,7 +171,7 @@ class OracleTable:
     def insert_or_assign(self, keys, values, scores=None) -> dict:
         k = _keys(keys)
         v = self._values(values, k.size)
-        s = None if scores is None else _keys(scores)
+        s = self._scores(scores)
         c = _Counts()
         _load().oracle_insert_or_assign(self._h, k.size, _ptr(k), _ptr(v), _ptr(s), ctypes.byref(c))
         return c.as_dict()
@@ -162,7 +179,7 @@ class OracleTable:
     def assign(self, keys, values, scores=None) -> dict:
         k = _keys(keys)
         v = self._values(values, k.size)
-        s = None if scores is None else _keys(scores)
+        s = self._scores(scores)
         c = _Counts()
         _load().oracle_assign(self._h, k.size, _ptr(k), _ptr(v), _ptr(s), ctypes.byref(c))
         return c.as_dict()
@@ -187,7 +204,7 @@ class OracleTable:
         """Returns (counts, (evicted keys, values, scores) sorted by key)."""
         k = _keys(keys)
         v = self._values(values, k.size)
-        s = None if scores is None else _keys(scores)
+        s = self._scores(scores)
         ek = np.zeros(max(k.size, 1), np.uint64)
         ev = np.zeros((max(k.size, 1), self.dim), np.float32)
         es = np.zeros(max(k.size, 1), np.uint64)
@@ -202,7 +219,7 @@ class OracleTable:
         """Returns (counts, values after the call, found flags)."""
         k = _keys(keys)
         v = self._values(values, k.size).copy().reshape(k.size, self.dim)
-        s = None if scores is None else _keys(scores)
+        s = self._scores(scores)
         found = np.zeros(k.size, np.uint8)
         c = _Counts()
         _load().oracle_find_or_insert(self._h, k.size, _ptr(k), _ptr(v), _ptr(s), _ptr(found),

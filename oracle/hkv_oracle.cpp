@@ -40,6 +40,31 @@
 //     untouched and reports found = 0.
 //  R9 slot positions are not modelled: a bucket is an unordered set of at
 //     most 128 entries; nothing observable depends on positions.
+//  R10 score policies.  HKV §3.3 ("Scoring policies") and §5 Exp #3c
+//     (Table 8) name five ScoreFunctor variants -- kLru, kLfu, kEpochLru,
+//     kEpochLfu, kCustomized -- but give none of their update rules.  A table
+//     is created with one of them, and the score a call writes for a key is:
+//       kCustomized  the caller's score; without scores the step counter (R7).
+//       kLru         the table clock.  The clock is the step counter, which
+//                    under this policy advances once per call that writes
+//                    scores (insert_or_assign, insert_and_evict,
+//                    find_or_insert, assign).  Callers pass no scores.
+//       kEpochLru    (epoch << 32) | (clock mod 2^32), clock as for kLru.
+//       kLfu         a frequency.  The caller's scores are per-occurrence
+//                    increments (1 each without scores); the increments of
+//                    all occurrences of a key in one call add up (R5 then
+//                    keeps the last occurrence's value).  A resident key
+//                    gets old + sum, an absent key competes with sum;
+//                    additions saturate at 2^64 - 1.
+//       kEpochLfu    (epoch << 32) | f with f the kLfu rule applied to the
+//                    low 32 bits of the old score, saturating at 2^32 - 1:
+//                    the count survives an epoch change, the epoch field
+//                    records the epoch of the last write.
+//     The epoch is a 32-bit value set on the table (0 at creation) and read
+//     when the call is issued.  find_or_insert leaves resident keys as they
+//     are under every policy (HKV §4.1).  With the epoch advanced once per
+//     call, both epoch policies rank like kLru across calls, which is the
+//     equality Table 8 shows for the three columns.
 //  The 8-bit digest only accelerates lookups and never changes a result
 //  (HKV §3.2), so the oracle does not model it.
 
@@ -100,10 +125,17 @@ struct Counts {
              erased = 0;
 };
 
+// R10: score policies.
+enum Policy : uint32_t { kCustomized = 0, kLru = 1, kLfu = 2, kEpochLru = 3, kEpochLfu = 4 };
+
+uint64_t add_sat64(uint64_t a, uint64_t b) { return a + b < a ? ~0ull : a + b; }
+
 struct Table {
     uint64_t num_buckets;
     uint32_t dim;
     bool dual;
+    uint32_t policy = kCustomized;                       // R10
+    uint32_t epoch = 0;                                  // R10
     uint64_t step = 1;                                   // R7
     std::unordered_map<uint64_t, Bucket> buckets;       // created on first use
     bool filtered = false;
@@ -228,6 +260,54 @@ struct Table {
         return false;
     }
 
+    // The score rule of one call (R7, R10).  `scores` are the caller's
+    // scores (kCustomized) or increments (kLfu, kEpochLfu).
+    struct ScoreRule {
+        uint32_t policy = kCustomized;
+        uint64_t clock = 0;      // the call's step / clock value
+        uint64_t epoch_hi = 0;   // epoch << 32
+        const uint64_t* scores = nullptr;
+        std::unordered_map<uint64_t, uint64_t> inc;   // kLfu kinds: summed increments
+
+        bool lfu() const { return policy == kLfu || policy == kEpochLfu; }
+        // Score of a key written by this call; `resident` with its old score.
+        uint64_t score(uint64_t i, uint64_t k, bool resident, uint64_t old) const {
+            switch (policy) {
+                case kLru: return clock;
+                case kEpochLru: return epoch_hi | (clock & 0xFFFFFFFFull);
+                case kLfu: {
+                    const uint64_t d = inc.at(k);
+                    return resident ? add_sat64(old, d) : d;
+                }
+                case kEpochLfu: {
+                    uint64_t f = add_sat64(resident ? (old & 0xFFFFFFFFull) : 0, inc.at(k));
+                    if (f > 0xFFFFFFFFull) f = 0xFFFFFFFFull;
+                    return epoch_hi | f;
+                }
+                default: return scores ? scores[i] : clock;
+            }
+        }
+    };
+
+    // Opens a call that writes scores: takes its clock and advances the step
+    // counter where the policy says so (R7, R10).
+    ScoreRule score_rule(uint64_t n, const uint64_t* keys, const uint64_t* scores) {
+        ScoreRule r;
+        r.policy = policy;
+        r.clock = step;
+        r.epoch_hi = static_cast<uint64_t>(epoch) << 32;
+        r.scores = scores;
+        if (policy == kLru || policy == kEpochLru || (policy == kCustomized && !scores)) ++step;
+        if (r.lfu()) {
+            for (uint64_t i = 0; i < n; ++i) {
+                if (is_reserved(keys[i])) continue;
+                uint64_t& d = r.inc[keys[i]];
+                d = add_sat64(d, scores ? scores[i] : 1);
+            }
+        }
+        return r;
+    }
+
     // update_resident = false gives find_or_insert's insertion step: resident
     // keys are left as they are.  evicted_out, when given, receives every
     // entry that was resident before the call and is displaced by it
@@ -236,16 +316,16 @@ struct Table {
                             const uint64_t* scores, bool update_resident = true,
                             std::vector<Victim>* evicted_out = nullptr) {
         Counts c;
-        uint64_t step_score = step;
+        const ScoreRule rule = score_rule(n, keys, scores);
         std::vector<uint64_t> idx = last_occurrences(n, keys, c);
         std::vector<uint64_t> absent;
         for (uint64_t i : idx) {                  // R6: resident keys first
             uint64_t k = keys[i];
             if (skip_for_filter(k, c)) continue;
-            uint64_t s = scores ? scores[i] : step_score;
             uint64_t b; int p;
             if (locate(k, &b, &p)) {              // HKV Algorithm 2, found branch
                 if (update_resident) {
+                    const uint64_t s = rule.score(i, k, true, at(b).scores[p]);
                     write_entry(at(b), p, k, s, values + i * dim);
                     ++c.updated;
                 }
@@ -260,7 +340,7 @@ struct Table {
         std::unordered_set<uint64_t> admitted;
         for (uint64_t i : absent) {
             uint64_t k = keys[i];
-            uint64_t s = scores ? scores[i] : step_score;
+            const uint64_t s = rule.score(i, k, false, 0);
             Victim victim;
             Outcome o = dual ? insert_dual(k, s, values + i * dim, &victim)
                              : insert_single(bucket1(k), k, s, values + i * dim, &victim);
@@ -275,12 +355,15 @@ struct Table {
         }
         c.admitted = admitted.size();
         c.rejected = absent.size() - admitted.size();
-        if (!scores) ++step;
         return c;
     }
 
     Counts assign(uint64_t n, const uint64_t* keys, const float* values, const uint64_t* scores) {
         Counts c;
+        // kCustomized without scores keeps the scores (and the step counter);
+        // every other case writes the policy's score (R10).
+        const bool keep = policy == kCustomized && !scores;
+        const ScoreRule rule = keep ? ScoreRule() : score_rule(n, keys, scores);
         std::vector<uint64_t> idx = last_occurrences(n, keys, c);
         for (uint64_t i : idx) {
             uint64_t k = keys[i];
@@ -290,7 +373,7 @@ struct Table {
             Bucket& bk = at(b);
             std::memcpy(&bk.values[static_cast<size_t>(p) * dim], values + i * dim,
                         sizeof(float) * dim);
-            if (scores) bk.scores[p] = scores[i];
+            if (!keep) bk.scores[p] = rule.score(i, k, true, bk.scores[p]);
             ++c.updated;
         }
         return c;
@@ -352,14 +435,20 @@ static void put(const Counts& c, oracle_counts* out) {
     out->erased = c.erased;
 }
 
-void* oracle_create(uint64_t num_buckets, uint32_t dim, int dual) {
-    if (num_buckets == 0 || dim == 0 || (dual && num_buckets < 2)) return nullptr;
+// policy: 0 kCustomized, 1 kLru, 2 kLfu, 3 kEpochLru, 4 kEpochLfu (R10).
+// Under kLru and kEpochLru the callers below must pass scores = NULL.
+void* oracle_create(uint64_t num_buckets, uint32_t dim, int dual, uint32_t policy) {
+    if (num_buckets == 0 || dim == 0 || (dual && num_buckets < 2) || policy > kEpochLfu)
+        return nullptr;
     Table* t = new Table();
     t->num_buckets = num_buckets;
     t->dim = dim;
     t->dual = dual != 0;
+    t->policy = policy;
     return t;
 }
+
+void oracle_set_epoch(void* h, uint32_t epoch) { static_cast<Table*>(h)->epoch = epoch; }
 
 void oracle_destroy(void* h) { delete static_cast<Table*>(h); }
 

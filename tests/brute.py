@@ -10,6 +10,9 @@ different form:
   key).  No slot, no arg-min loop, no eviction step.
 * dual-bucket mode replays HierarchicalKV §3.4 (Algorithm 3) key by key on
   Python dicts.
+* score policies (kLru, kLfu, kEpochLru, kEpochLfu, kCustomized; HKV §3.3 and
+  Table 8 name them, the update rules are the oracle's reading R10) are
+  computed with Python integers, saturation as a plain ``min``.
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ import numpy as np
 MASK = (1 << 64) - 1
 RESERVED_LO = 0xFFFFFFFFFFFFFFF0
 SLOTS = 128
+CUSTOMIZED, LRU, LFU, EPOCH_LRU, EPOCH_LFU = range(5)
+LOW32 = (1 << 32) - 1
 
 
 def fmix64(h: int) -> int:
@@ -31,10 +36,12 @@ def fmix64(h: int) -> int:
 
 
 class BruteTable:
-    def __init__(self, num_buckets: int, dim: int, dual: bool = False):
+    def __init__(self, num_buckets: int, dim: int, dual: bool = False, policy: int = CUSTOMIZED):
         self.B = num_buckets
         self.dim = dim
         self.dual = dual
+        self.policy = policy
+        self.epoch = 0
         self.step = 1
         # bucket -> {key: (score, tuple(values))}
         self.bk = {b: {} for b in range(num_buckets)}
@@ -70,6 +77,29 @@ class BruteTable:
     def residents(self):
         return {k for b in self.bk.values() for k in b}
 
+    def _rule(self, keys, scores):
+        """score(i, key, old score or None) for one call that writes scores."""
+        pol, clock, hi = self.policy, self.step, self.epoch << 32
+        if pol in (LRU, EPOCH_LRU) or (pol == CUSTOMIZED and scores is None):
+            self.step += 1
+        total = {}
+        if pol in (LFU, EPOCH_LFU):
+            for i, k in enumerate(keys):
+                if k < RESERVED_LO:
+                    total[k] = total.get(k, 0) + (int(scores[i]) if scores is not None else 1)
+
+        def score(i, k, old):
+            if pol == LRU:
+                return clock
+            if pol == EPOCH_LRU:
+                return hi + clock % (1 << 32)
+            if pol == LFU:
+                return min((0 if old is None else old) + total[k], MASK)
+            if pol == EPOCH_LFU:
+                return hi + min((0 if old is None else old % (1 << 32)) + total[k], LOW32)
+            return int(scores[i]) if scores is not None else clock
+        return score
+
     # -- operations --------------------------------------------------------
     def insert_or_assign(self, keys, values, scores=None, update_resident=True, evicted_out=None):
         """update_resident=False: find_or_insert's insertion step (resident
@@ -78,7 +108,7 @@ class BruteTable:
         keys = [int(k) for k in keys]
         values = np.asarray(values, np.float32).reshape(len(keys), self.dim)
         order, reserved = self._last(keys)
-        s_of = (lambda i: int(scores[i])) if scores is not None else (lambda i: self.step)
+        score = self._rule(keys, scores)
         before = self.residents()
         updated = 0
         absent = []
@@ -87,18 +117,18 @@ class BruteTable:
             b = self.where(k)
             if b is not None:
                 if update_resident:
-                    self.bk[b][k] = (s_of(i), tuple(values[i].tolist()))
+                    self.bk[b][k] = (score(i, k, self.bk[b][k][0]), tuple(values[i].tolist()))
                     updated += 1
             else:
                 absent.append(i)
         snapshot = {k: sv for d in self.bk.values() for k, sv in d.items()}
         if self.dual:
             for i in absent:
-                self._dual_insert(keys[i], s_of(i), tuple(values[i].tolist()))
+                self._dual_insert(keys[i], score(i, keys[i], None), tuple(values[i].tolist()))
         else:
             for i in absent:
                 k = keys[i]
-                self.bk[self.b1(k)][k] = (s_of(i), tuple(values[i].tolist()))
+                self.bk[self.b1(k)][k] = (score(i, k, None), tuple(values[i].tolist()))
             for b, d in self.bk.items():
                 if len(d) > SLOTS:
                     top = sorted(d.items(), key=lambda kv: (kv[1][0], kv[0]), reverse=True)[:SLOTS]
@@ -107,8 +137,6 @@ class BruteTable:
         if evicted_out is not None:
             evicted_out.extend((k, snapshot[k][0], snapshot[k][1]) for k in sorted(before - after))
         absent_keys = {keys[i] for i in absent}
-        if scores is None:
-            self.step += 1
         return {
             "updated": updated,
             "admitted": len(absent_keys & after),
@@ -135,12 +163,14 @@ class BruteTable:
         keys = [int(k) for k in keys]
         values = np.asarray(values, np.float32).reshape(len(keys), self.dim)
         order, _ = self._last(keys)
+        keep = self.policy == CUSTOMIZED and scores is None
+        score = None if keep else self._rule(keys, scores)
         for i in order:
             b = self.where(keys[i])
             if b is None:
                 continue
             old = self.bk[b][keys[i]]
-            s = int(scores[i]) if scores is not None else old[0]
+            s = old[0] if keep else score(i, keys[i], old[0])
             self.bk[b][keys[i]] = (s, tuple(values[i].tolist()))
 
     def erase(self, keys):
