@@ -29,6 +29,13 @@ LIB_PATH = os.path.join(PKG, "libhkv.so")
 HKV_MODE_SINGLE = 0
 HKV_MODE_DUAL = 1
 HKV_MODE_TIERED = 2
+# score policies, ORed into the mode (HKV §3.3; Table 8 names)
+HKV_POLICY_CUSTOMIZED = 0x00
+HKV_POLICY_LRU = 0x10
+HKV_POLICY_LFU = 0x20
+HKV_POLICY_EPOCH_LRU = 0x30
+HKV_POLICY_EPOCH_LFU = 0x40
+HKV_POLICY_MASK = 0xF0
 HKV_OK = 0
 HKV_ERR_INVALID = -1
 HKV_ERR_OOM = -2
@@ -44,6 +51,7 @@ EXPORTS = (
     "hkv_size", "hkv_export", "hkv_get_error_counts", "hkv_get_op_counts",
     "hkv_reset_op_counts", "hkv_get_info", "hkv_status_string", "hkv_insert_or_assign_noalloc",
     "hkv_insert_and_evict", "hkv_find_or_insert", "hkv_contains", "hkv_find_ptr",
+    "hkv_set_epoch",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -103,6 +111,7 @@ def load(path: str = LIB_PATH):
         "hkv_get_op_counts": [vp, ctypes.POINTER(OpCounts)],
         "hkv_reset_op_counts": [vp],
         "hkv_get_info": [vp, ctypes.POINTER(Info)],
+        "hkv_set_epoch": [vp, u32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -225,6 +234,10 @@ def hkv_get_info(table):
     i = Info()
     st = load().hkv_get_info(table, ctypes.byref(i))
     return st, {f: getattr(i, f) for f, _ in Info._fields_}
+
+
+def hkv_set_epoch(table, epoch):
+    return load().hkv_set_epoch(table, int(epoch) & 0xFFFFFFFF)
 
 
 def hkv_status_string(status):
@@ -377,3 +390,6 @@ class HashTable:
         st, i = hkv_get_info(self.handle)
         _check(st, "hkv_get_info")
         return i
+
+    def set_epoch(self, epoch):
+        _check(hkv_set_epoch(self.handle, epoch), "hkv_set_epoch")

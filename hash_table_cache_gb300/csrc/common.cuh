@@ -51,6 +51,54 @@ struct TableView {
   DeviceStats* stats;
 };
 
+// Score policies (HKV §3.3 "Scoring policies"; Table 8 names kCustomized,
+// kLru, kLfu, kEpochLru, kEpochLfu).  Values are the policy field of the
+// table mode shifted down by 4.
+enum Policy : uint32_t { kCustomized = 0, kLru = 1, kLfu = 2, kEpochLru = 3, kEpochLfu = 4 };
+
+// How one call computes the scores it writes; passed by value.
+struct ScoreRule {
+  const uint64_t* in;  // caller scores (kCustomized) or increments (LFU kinds); may be null
+  uint64_t clock;      // the call's step counter value
+  uint64_t epoch_hi;   // epoch << 32
+  uint32_t policy;
+  __host__ __device__ bool lfu() const { return policy == kLfu || policy == kEpochLfu; }
+};
+
+__device__ __forceinline__ uint64_t add_sat64(uint64_t a, uint64_t b) {
+  const uint64_t c = a + b;
+  return c < a ? ~0ull : c;
+}
+
+// Score written for batch entry e.  `inc` is the entry's summed increment
+// (LFU kinds); `old` the resident entry's score when `resident`.
+__device__ __forceinline__ uint64_t policy_score(const ScoreRule& r, uint64_t e, uint64_t inc,
+                                                 bool resident, uint64_t old) {
+  switch (r.policy) {
+    case kLru: return r.clock;
+    case kEpochLru: return r.epoch_hi | (r.clock & 0xFFFFFFFFull);
+    case kLfu: return resident ? add_sat64(old, inc) : inc;
+    case kEpochLfu: {
+      const uint64_t f = add_sat64(resident ? (old & 0xFFFFFFFFull) : 0ull, inc);
+      return r.epoch_hi | (f > 0xFFFFFFFFull ? 0xFFFFFFFFull : f);
+    }
+    default: return r.in ? r.in[e] : r.clock;
+  }
+}
+
+// Saturating atomic add of a 64-bit counter (lock-free: a failed CAS means
+// another thread's add went through).
+__device__ __forceinline__ void atomic_add_sat64(uint64_t* p, uint64_t v) {
+  unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(q);
+  while (true) {
+    const unsigned long long nv = add_sat64(old, v);
+    const unsigned long long seen = atomicCAS(q, old, nv);
+    if (seen == old) return;
+    old = seen;
+  }
+}
+
 // H(k): the 64-bit MurmurHash3 finalizer (HKV §3.1 names a Murmur3-derived
 // hash; the finalizer is the published 64-bit mixing step).
 __host__ __device__ __forceinline__ uint64_t hash64(uint64_t h) {

@@ -21,6 +21,8 @@ struct UpsertScratch {
   uint8_t* mark;        // single mode, sparse batches: one byte per table bucket,
                         // 1 = holds batch keys (null for dense batches)
   uint32_t* group;      // dual mode: indices of the batch's absent keys
+  uint64_t* inc;        // LFU policies: summed increments per map entry,
+                        // 0-initialised (null under the other policies)
 };
 
 // What a call needs scratch for.
@@ -28,8 +30,10 @@ enum class ScratchKind { kSingleUpsert, kDualUpsert, kAssign };
 
 // Bytes of scratch a call of n keys needs, and the carving of one allocation
 // into the UpsertScratch arrays.
-size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind);
-UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind);
+// `lfu`: the table's policy sums increments (kLfu, kEpochLfu).
+size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind, bool lfu);
+UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind,
+                                   bool lfu);
 // Enqueue the clears the scratch needs before use.
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st);
@@ -54,12 +58,13 @@ struct UpsertExtra {
 };
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
-                          const uint64_t* keys, const float* values, const uint64_t* scores,
-                          uint64_t step_score, cudaStream_t st, const UpsertExtra& ex = UpsertExtra());
+                          const uint64_t* keys, const float* values, const ScoreRule& rule,
+                          cudaStream_t st, const UpsertExtra& ex = UpsertExtra());
 
+// keep_scores: write values only (kCustomized without caller scores).
 cudaError_t launch_assign(const TableView& t, const UpsertScratch& s, uint64_t n,
-                          const uint64_t* keys, const float* values, const uint64_t* scores,
-                          cudaStream_t st);
+                          const uint64_t* keys, const float* values, const ScoreRule& rule,
+                          bool keep_scores, cudaStream_t st);
 
 cudaError_t launch_erase(const TableView& t, uint64_t n, const uint64_t* keys, cudaStream_t st);
 

@@ -135,7 +135,9 @@ struct hkv_table {
   float* host_slab = nullptr;  // host address of the mapped value slab
   cudaMemPool_t pool = nullptr;
   cudaStream_t aux = nullptr;
-  uint64_t step = 1;
+  uint64_t step = 1;       // step counter / clock of the score policies
+  uint32_t policy = 0;     // hkv::Policy
+  uint32_t epoch = 0;
   RoleTracker roles;
   std::mutex mu;
 };
@@ -160,6 +162,32 @@ void release(hkv_table* t) {
 
 bool batch_ok(hkv_table* t, uint64_t n) { return t && n <= HKV_MAX_BATCH; }
 
+bool clock_policy(const hkv_table* t) {
+  return t->policy == hkv::kLru || t->policy == hkv::kEpochLru;
+}
+
+// Clock-driven policies take no caller scores.
+bool scores_ok(const hkv_table* t, const uint64_t* scores) {
+  return !(scores && clock_policy(t));
+}
+
+bool lfu_policy(const hkv_table* t) {
+  return t->policy == hkv::kLfu || t->policy == hkv::kEpochLfu;
+}
+
+// The score rule of a call that writes scores, taken when the call is issued:
+// it reads the clock and the epoch and advances the step counter where the
+// policy says so (kCustomized without scores, the clock policies always).
+hkv::ScoreRule take_rule(hkv_table* t, const uint64_t* scores) {
+  hkv::ScoreRule r{};
+  r.in = scores;
+  r.clock = t->step;
+  r.epoch_hi = static_cast<uint64_t>(t->epoch) << 32;
+  r.policy = t->policy;
+  if (clock_policy(t) || (t->policy == hkv::kCustomized && !scores)) ++t->step;
+  return r;
+}
+
 // Common frame of a batched call: lock, select the device, order by role,
 // run `body`, record the role event.
 template <class F>
@@ -182,10 +210,10 @@ namespace hkv {
 int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
                        const uint64_t* scores, void* stream,
                        cudaError_t (*get_scratch)(int, void**)) {
-  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (!batch_ok(t, n) || !scores_ok(t, scores)) return HKV_ERR_INVALID;
   if (n && (!keys || !values)) return HKV_ERR_INVALID;
   const ScratchKind kind = t->v.dual ? ScratchKind::kDualUpsert : ScratchKind::kSingleUpsert;
-  if (upsert_scratch_bytes(n, t->v.num_buckets, kind) > HKV_NOALLOC_SCRATCH_BYTES)
+  if (upsert_scratch_bytes(n, t->v.num_buckets, kind, lfu_policy(t)) > HKV_NOALLOC_SCRATCH_BYTES)
     return HKV_ERR_INVALID;
   std::lock_guard<std::mutex> lk(t->mu);
   DeviceGuard g(t->device);
@@ -195,12 +223,11 @@ int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const flo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = t->roles.before(Role::kInserter, s);  // waits only: records no event
   if (e != cudaSuccess) return from_cuda(e);
-  const uint64_t step_score = t->step;
-  if (!scores) ++t->step;
+  const ScoreRule rule = take_rule(t, scores);
   if (n == 0) return HKV_OK;
-  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, kind);
+  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, kind, lfu_policy(t));
   e = clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
-  if (e == cudaSuccess) e = launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
+  if (e == cudaSuccess) e = launch_upsert(t->v, sc, n, keys, values, rule, s);
   return from_cuda(e);
 }
 
@@ -213,7 +240,9 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
   if (!out) return HKV_ERR_INVALID;
   *out = nullptr;
   if (capacity == 0 || capacity % hkv::kSlots != 0 || dim == 0) return HKV_ERR_INVALID;
-  if (mode & ~static_cast<uint32_t>(HKV_MODE_DUAL | HKV_MODE_TIERED)) return HKV_ERR_INVALID;
+  if (mode & ~static_cast<uint32_t>(HKV_MODE_DUAL | HKV_MODE_TIERED | HKV_POLICY_MASK))
+    return HKV_ERR_INVALID;
+  if ((mode & HKV_POLICY_MASK) > HKV_POLICY_EPOCH_LFU) return HKV_ERR_INVALID;
   const uint64_t nb = capacity / hkv::kSlots;
   if (nb >= 0xFFFFFFFFull) return HKV_ERR_INVALID;
   const bool dual = (mode & HKV_MODE_DUAL) != 0;
@@ -226,6 +255,7 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
   if (!t) return HKV_ERR_OOM;
   t->device = device;
   t->mode = mode;
+  t->policy = (mode & HKV_POLICY_MASK) >> 4;
   t->capacity = capacity;
   DeviceGuard g(device);
 
@@ -300,7 +330,7 @@ namespace {
 // the same stream after the kernels, so concurrent calls never share it.
 hkv_status scratch_call(hkv_table* t, cudaStream_t s, uint64_t n, hkv::ScratchKind kind,
                         void** mem) {
-  const size_t bytes = hkv::upsert_scratch_bytes(n, t->v.num_buckets, kind);
+  const size_t bytes = hkv::upsert_scratch_bytes(n, t->v.num_buckets, kind, lfu_policy(t));
   cudaError_t e = cudaMallocFromPoolAsync(mem, bytes, t->pool, s);
   return from_cuda(e);
 }
@@ -309,20 +339,19 @@ hkv_status scratch_call(hkv_table* t, cudaStream_t s, uint64_t n, hkv::ScratchKi
 
 hkv_status hkv_insert_or_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
                                 const uint64_t* scores, void* stream) {
-  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (!batch_ok(t, n) || !scores_ok(t, scores)) return HKV_ERR_INVALID;
   if (n && (!keys || !values)) return HKV_ERR_INVALID;
   return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
-    const uint64_t step_score = t->step;
-    if (!scores) ++t->step;
+    const hkv::ScoreRule rule = take_rule(t, scores);
     if (n == 0) return HKV_OK;
     const hkv::ScratchKind kind =
         t->v.dual ? hkv::ScratchKind::kDualUpsert : hkv::ScratchKind::kSingleUpsert;
     void* mem = nullptr;
     hkv_status st = scratch_call(t, s, n, kind, &mem);
     if (st != HKV_OK) return st;
-    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, kind);
+    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, kind, lfu_policy(t));
     cudaError_t e = hkv::clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
-    if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, scores, step_score, s);
+    if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, rule, s);
     cudaError_t f = cudaFreeAsync(mem, s);
     return from_cuda(e != cudaSuccess ? e : f);
   });
@@ -353,17 +382,16 @@ namespace {
 hkv_status upsert_variant(hkv_table* t, cudaStream_t s, uint64_t n, const uint64_t* keys,
                           const float* values, const uint64_t* scores,
                           const hkv::UpsertExtra& ex) {
-  const uint64_t step_score = t->step;
-  if (!scores) ++t->step;
+  const hkv::ScoreRule rule = take_rule(t, scores);
   if (n == 0) return HKV_OK;
   void* mem = nullptr;
   hkv_status st = scratch_call(t, s, n, hkv::ScratchKind::kSingleUpsert, &mem);
   if (st != HKV_OK) return st;
-  hkv::UpsertScratch sc =
-      hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, hkv::ScratchKind::kSingleUpsert);
+  hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets,
+                                                    hkv::ScratchKind::kSingleUpsert, lfu_policy(t));
   cudaError_t e =
       hkv::clear_upsert_scratch(sc, t->v.num_buckets, hkv::ScratchKind::kSingleUpsert, s);
-  if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, scores, step_score, s, ex);
+  if (e == cudaSuccess) e = hkv::launch_upsert(t->v, sc, n, keys, values, rule, s, ex);
   cudaError_t f = cudaFreeAsync(mem, s);
   return from_cuda(e != cudaSuccess ? e : f);
 }
@@ -375,7 +403,7 @@ hkv_status hkv_insert_and_evict(hkv_table* t, uint64_t n, const uint64_t* keys,
                                 uint64_t* evicted_keys_out, float* evicted_values_out,
                                 uint64_t* evicted_scores_out, uint64_t* evicted_count_out,
                                 void* stream) {
-  if (!batch_ok(t, n) || t->v.dual) return HKV_ERR_INVALID;
+  if (!batch_ok(t, n) || t->v.dual || !scores_ok(t, scores)) return HKV_ERR_INVALID;
   if (n && (!keys || !values)) return HKV_ERR_INVALID;
   if (!evicted_keys_out || !evicted_count_out) return HKV_ERR_INVALID;
   return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
@@ -392,7 +420,7 @@ hkv_status hkv_insert_and_evict(hkv_table* t, uint64_t n, const uint64_t* keys,
 
 hkv_status hkv_find_or_insert(hkv_table* t, uint64_t n, const uint64_t* keys, float* values_inout,
                               const uint64_t* scores, uint8_t* found_out, void* stream) {
-  if (!batch_ok(t, n) || t->v.dual) return HKV_ERR_INVALID;
+  if (!batch_ok(t, n) || t->v.dual || !scores_ok(t, scores)) return HKV_ERR_INVALID;
   if (n && (!keys || !values_inout || !found_out)) return HKV_ERR_INVALID;
   return run_call(t, Role::kInserter, stream, [&](cudaStream_t s) -> hkv_status {
     hkv::UpsertExtra ex;
@@ -405,18 +433,21 @@ hkv_status hkv_find_or_insert(hkv_table* t, uint64_t n, const uint64_t* keys, fl
 
 hkv_status hkv_assign(hkv_table* t, uint64_t n, const uint64_t* keys, const float* values,
                       const uint64_t* scores, void* stream) {
-  if (!batch_ok(t, n)) return HKV_ERR_INVALID;
+  if (!batch_ok(t, n) || !scores_ok(t, scores)) return HKV_ERR_INVALID;
   if (n && (!keys || !values)) return HKV_ERR_INVALID;
   return run_call(t, Role::kUpdater, stream, [&](cudaStream_t s) -> hkv_status {
+    // kCustomized without scores keeps the scores and the step counter
+    const bool keep = t->policy == hkv::kCustomized && !scores;
+    const hkv::ScoreRule rule = keep ? hkv::ScoreRule{} : take_rule(t, scores);
     if (n == 0) return HKV_OK;
     void* mem = nullptr;
     hkv_status st = scratch_call(t, s, n, hkv::ScratchKind::kAssign, &mem);
     if (st != HKV_OK) return st;
-    hkv::UpsertScratch sc =
-        hkv::carve_upsert_scratch(mem, n, t->v.num_buckets, hkv::ScratchKind::kAssign);
+    hkv::UpsertScratch sc = hkv::carve_upsert_scratch(mem, n, t->v.num_buckets,
+                                                      hkv::ScratchKind::kAssign, lfu_policy(t));
     cudaError_t e =
         hkv::clear_upsert_scratch(sc, t->v.num_buckets, hkv::ScratchKind::kAssign, s);
-    if (e == cudaSuccess) e = hkv::launch_assign(t->v, sc, n, keys, values, scores, s);
+    if (e == cudaSuccess) e = hkv::launch_assign(t->v, sc, n, keys, values, rule, keep, s);
     cudaError_t f = cudaFreeAsync(mem, s);
     return from_cuda(e != cudaSuccess ? e : f);
   });
@@ -498,6 +529,13 @@ hkv_status hkv_reset_op_counts(hkv_table* t) {
                    offsetof(hkv::DeviceStats, size) - offsetof(hkv::DeviceStats, updated));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return from_cuda(e);
+}
+
+hkv_status hkv_set_epoch(hkv_table* t, uint32_t epoch) {
+  if (!t) return HKV_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(t->mu);
+  t->epoch = epoch;
+  return HKV_OK;
 }
 
 hkv_status hkv_get_info(hkv_table* t, hkv_info* out) {

@@ -28,6 +28,8 @@
 // place by a tile kernel, then each absent key is placed by one warp holding
 // locks on both candidate buckets (taken in increasing bucket order, bounded
 // spin).
+#include <cstddef>
+
 #include "launch.h"
 
 namespace hkv {
@@ -55,19 +57,30 @@ __device__ __forceinline__ uint32_t map_find(const uint64_t* mkeys, uint32_t mas
   return kNone;
 }
 
-__device__ __forceinline__ bool is_last_occurrence(const UpsertScratch& sc, uint64_t key,
-                                                   uint64_t i) {
+// Map entry of `key` when batch index i is its last occurrence, else kNone.
+__device__ __forceinline__ uint32_t last_occurrence_slot(const UpsertScratch& sc, uint64_t key,
+                                                         uint64_t i) {
   const uint32_t mask = sc.map_size - 1;
   const uint32_t s = map_find(sc.map_keys, mask, key);
-  return s != kNone && sc.map_keys[s] == key && sc.map_idx[s] == static_cast<uint32_t>(i) + 1;
+  const bool last =
+      s != kNone && sc.map_keys[s] == key && sc.map_idx[s] == static_cast<uint32_t>(i) + 1;
+  return last ? s : kNone;
+}
+
+// Summed increment of a deduplicated entry (LFU policies; 0 otherwise).
+__device__ __forceinline__ uint64_t entry_inc(const UpsertScratch& sc, uint32_t slot) {
+  return sc.inc ? sc.inc[slot] : 0ull;
 }
 
 // ---------------------------------------------------------------------------
 // 1. dedup: map[key] = max batch index + 1.  Lanes of a warp holding the same
-// key are merged first (the highest lane holds the largest index).
+// key are merged first (the highest lane holds the largest index).  Under the
+// LFU policies every occurrence adds its increment (inc_in[i], or 1) to the
+// entry's sum.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) dedup_insert_kernel(UpsertScratch sc, uint64_t n,
                                                                 const uint64_t* keys,
+                                                                const uint64_t* inc_in,
                                                                 DeviceStats* stats) {
   const unsigned lane = lane_id();
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
@@ -81,7 +94,9 @@ __global__ void __launch_bounds__(kThreads) dedup_insert_kernel(UpsertScratch sc
     const bool valid = active && !is_reserved(k);
     if (active && !valid) ++reserved;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, k);
-    const bool leader = valid && static_cast<unsigned>(31 - __clz(peers)) == lane;
+    const unsigned lead = static_cast<unsigned>(31 - __clz(peers));
+    const bool leader = valid && lead == lane;
+    uint32_t slot = kNone;
     if (leader) {
       uint32_t s = map_home(k, mask);
       for (uint32_t p = 0; p <= mask; ++p) {
@@ -89,10 +104,15 @@ __global__ void __launch_bounds__(kThreads) dedup_insert_kernel(UpsertScratch sc
             reinterpret_cast<unsigned long long*>(sc.map_keys + s), kEmptyKey, k);
         if (prev == kEmptyKey || prev == k) {
           atomicMax(sc.map_idx + s, static_cast<uint32_t>(i) + 1);
+          slot = s;
           break;
         }
         s = (s + 1) & mask;
       }
+    }
+    if (sc.inc) {  // warp-uniform
+      slot = __shfl_sync(0xFFFFFFFFu, slot, lead);
+      if (valid && slot != kNone) atomic_add_sat64(sc.inc + slot, inc_in ? inc_in[i] : 1ull);
     }
   }
   warp_add(&stats->reserved, reserved);
@@ -119,7 +139,8 @@ __device__ __forceinline__ uint64_t stage_home(uint64_t h, uint64_t lo, uint64_t
 constexpr int kStageKeysPerThread = 1;
 
 __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScratch sc, uint64_t n,
-                                                         const uint64_t* keys) {
+                                                         const uint64_t* keys,
+                                                         const uint64_t* inc_in) {
   constexpr int U = kStageKeysPerThread;
   const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
@@ -158,6 +179,8 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
         pv = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + p), kEmptyKey, k[u]);
       }
       atomicMax(sc.map_idx + p, static_cast<uint32_t>(i0 + u * stride) + 1);
+      // LFU policies: every occurrence adds its increment to the entry's sum
+      if (sc.inc) atomic_add_sat64(sc.inc + p, inc_in ? inc_in[i0 + u * stride] : 1ull);
       // Sparse batches mark the buckets they touch (plain store) so that the
       // processing kernel skips the others without reading them; dense
       // batches skip the marks, which would only collide.
@@ -182,18 +205,30 @@ __device__ __forceinline__ bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2,
 // ---------------------------------------------------------------------------
 constexpr int kWin = 4;  // stage chunks (32 positions each) held in registers
 
-struct BucketStage {
-  uint64_t ekey[kWin * 32];  // the bucket's batch entries, compacted
-  uint32_t eidx[kWin * 32];
-  uint64_t key[kSlots];
-  uint64_t score[kSlots];
-  uint32_t occ[kSlots];
-  uint32_t dig[kSlots / 4];
-  uint32_t fresh[kSlots / 32];
-  uint32_t dhead[256];   // digest -> first slot carrying it (0xFF: none)
-  uint8_t dnext[kSlots];  // next slot with the same digest (0xFF: end)
-  uint8_t list[kSlots];  // free-slot list, later the dirty-slot list
+// Arrays read or written with 16-byte vector accesses are aligned to 16.
+template <bool kLfu>
+struct alignas(16) BucketStage {
+  alignas(16) uint64_t ekey[kWin * 32];  // the bucket's batch entries, compacted
+  alignas(16) uint32_t eidx[kWin * 32];
+  alignas(16) uint64_t key[kSlots];
+  alignas(16) uint64_t score[kSlots];
+  alignas(16) uint32_t occ[kSlots];
+  alignas(16) uint32_t dig[kSlots / 4];
+  alignas(16) uint32_t fresh[kSlots / 32];
+  alignas(16) uint32_t dhead[256];  // digest -> first slot carrying it (0xFF: none)
+  uint8_t dnext[kSlots];            // next slot with the same digest (0xFF: end)
+  uint8_t list[kSlots];             // free-slot list, later the dirty-slot list
+  alignas(16) uint64_t einc[kLfu ? kWin * 32 : 2];  // summed increments (LFU policies)
 };
+#define HKV_STAGE_ALIGNED(L)                                                                     \
+  static_assert(offsetof(BucketStage<L>, key) % 16 == 0 &&                                     \
+                    offsetof(BucketStage<L>, score) % 16 == 0 &&                               \
+                    offsetof(BucketStage<L>, occ) % 16 == 0 &&                                 \
+                    offsetof(BucketStage<L>, dhead) % 16 == 0 && sizeof(BucketStage<L>) % 16 == 0, \
+                "vector-accessed stage arrays must be 16-byte aligned")
+HKV_STAGE_ALIGNED(false);
+HKV_STAGE_ALIGNED(true);
+#undef HKV_STAGE_ALIGNED
 
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
@@ -224,13 +259,21 @@ __device__ __forceinline__ uint64_t warp_min_u64(uint64_t v, bool valid, unsigne
   return (static_cast<uint64_t>(mh) << 32) | ml;
 }
 
+// kLfu: the table sums increments (kLfu, kEpochLfu).  Otherwise every key of
+// the call gets rule.in[e] or the constant rule.clock (the host folds the
+// clock policies into that constant).
+template <bool kLfu>
 __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
-    const uint64_t* scores_in, uint64_t step_score, bool vec, UpsertExtra ex) {
+    ScoreRule rule, bool vec, UpsertExtra ex) {
   (void)keys_in;  // entry keys come from the stage
-  __shared__ BucketStage stage_all[kThreads / 32];
+  __shared__ BucketStage<kLfu> stage_all[kThreads / 32];
   const unsigned lane = lane_id();
-  BucketStage& st = stage_all[threadIdx.x >> 5];
+  BucketStage<kLfu>& st = stage_all[threadIdx.x >> 5];
+  auto score_of = [&](uint32_t e, uint64_t inc, bool resident, uint64_t old) -> uint64_t {
+    if (kLfu) return policy_score(rule, e, inc, resident, old);
+    return rule.in ? rule.in[e] : rule.clock;
+  };
   const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   const uint64_t nb = t.num_buckets;
   const unsigned sub = lane & 7u;
@@ -306,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     // Phase A (Algorithm 2, found branch): a resident key gets its new value
     // and score.  The entry lane scans the staged digest line and confirms
     // matches against the staged keys.  Returns whether the entry hit.
-    auto phase_a = [&](uint32_t e, uint64_t ke) -> bool {
+    auto phase_a = [&](uint32_t e, uint64_t ke, uint64_t inc) -> bool {
       int hs = -1;
       if (e != kNone) {
         // walk the slots whose digest equals the key's (HKV Algorithm 1's
@@ -321,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         }
         if (hs >= 0 && ex.update_resident) {
           st.occ[hs] = e;
-          st.score[hs] = scores_in ? scores_in[e] : step_score;
+          st.score[hs] = score_of(e, inc, true, st.score[hs]);
         }
       }
       const unsigned hm = __ballot_sync(0xFFFFFFFFu, hs >= 0);
@@ -339,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     // Extracted absent keys are rejected; the absent keys left take the slots
     // of the extracted entries.
     uint32_t nfree = 0, used = 0;
-    auto phase_b = [&](uint32_t e, uint64_t ke, bool miss) {
-      const uint64_t se = miss ? (scores_in ? scores_in[e] : step_score) : 0;
+    auto phase_b = [&](uint32_t e, uint64_t ke, bool miss, uint64_t inc) {
+      const uint64_t se = miss ? score_of(e, inc, false, 0) : 0;
       const unsigned mm = __ballot_sync(0xFFFFFFFFu, miss);
       if (!mm) return;
       const uint32_t rank = used + __popc(mm & lanemask_lt());
@@ -494,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
           const uint32_t p = ne + __popc(m & lanemask_lt());
           st.ekey[p] = wk[w];
           st.eidx[p] = we[w];
+          if (kLfu) st.einc[p] = scr.inc[(lo + 32ull * w + lane) & smask];
         }
         ne += __popc(m);
       }
@@ -503,7 +547,9 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
 #pragma unroll 1
       for (uint32_t c = 0; 32u * c < ne; ++c) {
         const bool v = 32u * c + lane < ne;
-        if (phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey))
+        const uint64_t inc = kLfu && v ? st.einc[32 * c + lane] : 0ull;
+        if (phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey,
+                    inc))
           hits |= 1u << c;
       }
       __syncwarp();
@@ -512,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       for (uint32_t c = 0; 32u * c < ne; ++c) {
         const bool v = 32u * c + lane < ne;
         const uint32_t e = v ? st.eidx[32 * c + lane] : kNone;
-        phase_b(e, v ? st.ekey[32 * c + lane] : kEmptyKey, v && !((hits >> c) & 1u));
+        const uint64_t inc = kLfu && v ? st.einc[32 * c + lane] : 0ull;
+        phase_b(e, v ? st.ekey[32 * c + lane] : kEmptyKey, v && !((hits >> c) & 1u), inc);
       }
     } else {
       // Long run: walk it chunk by chunk from the stage, marking hits there.
@@ -523,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         const uint64_t key = scr.map_keys[j];
         const uint32_t raw = scr.map_idx[j];
         const uint32_t e = entry_of(c, key, raw);
-        if (phase_a(e, key)) scr.map_idx[j] = raw | kHitMark;
+        if (phase_a(e, key, kLfu && e != kNone ? entry_inc(scr, static_cast<uint32_t>(j)) : 0ull))
+          scr.map_idx[j] = raw | kHitMark;
         nch = c + 1;
       }
       __syncwarp();
@@ -534,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         const uint64_t key = scr.map_keys[j];
         const uint32_t raw = scr.map_idx[j];
         const uint32_t e = entry_of(c, key, raw);
-        phase_b(e, key, e != kNone && !(raw & kHitMark));
+        phase_b(e, key, e != kNone && !(raw & kHitMark),
+                kLfu && e != kNone ? entry_inc(scr, static_cast<uint32_t>(j)) : 0ull);
       }
     }
     __syncwarp();
@@ -594,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
 // miss list.  One 8-lane tile per key.
 __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
-    const uint64_t* scores, uint64_t step_score, bool vec) {
+    ScoreRule rule, bool vec) {
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
@@ -603,7 +652,9 @@ __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
   for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
        i += tiles) {
     const uint64_t k = keys[i];
-    if (is_reserved(k) || !is_last_occurrence(sc, k, i)) continue;
+    if (is_reserved(k)) continue;
+    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    if (ms == kNone) continue;
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
     uint64_t b = bucket_of_hash(t, h);
@@ -616,7 +667,8 @@ __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
       const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
       tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
       if (sub == 0) {
-        *score_at(t, row) = scores ? scores[i] : step_score;
+        uint64_t* sp = score_at(t, row);
+        *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
         ++upd;
       }
     } else if (sub == 0) {
@@ -664,8 +716,8 @@ __device__ __forceinline__ uint32_t warp_argmin(const uint64_t* s, const uint64_
 
 // Absent keys: one warp per key, both candidate buckets locked.
 __global__ void __launch_bounds__(kThreads) dual_place_kernel(
-    TableView t, UpsertScratch sc, const uint64_t* keys, const float* values,
-    const uint64_t* scores, uint64_t step_score, bool vec) {
+    TableView t, UpsertScratch sc, const uint64_t* keys, const float* values, ScoreRule rule,
+    bool vec) {
   const unsigned lane = lane_id();
   const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   const uint32_t nmiss = *(volatile uint32_t*)(sc.cursor + 1);
@@ -674,7 +726,8 @@ __global__ void __launch_bounds__(kThreads) dual_place_kernel(
        w += nwarps) {
     const uint32_t i = sc.group[w];
     const uint64_t k = keys[i];
-    const uint64_t s = scores ? scores[i] : step_score;
+    const uint64_t inc = sc.inc ? sc.inc[map_find(sc.map_keys, sc.map_size - 1, k)] : 0ull;
+    const uint64_t s = policy_score(rule, i, inc, false, 0);
     const uint64_t h = hash64(k);
     const uint64_t b1 = bucket_of_hash(t, h);
     const uint64_t b2 = bucket2_of(t, k, b1);
@@ -815,7 +868,8 @@ __global__ void dual_finish_kernel(TableView t, UpsertScratch sc) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScratch sc, uint64_t n,
                                                           const uint64_t* keys, const float* values,
-                                                          const uint64_t* scores, bool vec) {
+                                                          ScoreRule rule, bool keep_scores,
+                                                          bool vec) {
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
@@ -824,7 +878,9 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScr
   for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
        i += tiles) {
     const uint64_t k = keys[i];
-    if (is_reserved(k) || !is_last_occurrence(sc, k, i)) continue;
+    if (is_reserved(k)) continue;
+    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    if (ms == kNone) continue;
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
     uint64_t b = bucket_of_hash(t, h);
@@ -837,7 +893,10 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScr
     const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
     tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
     if (sub == 0) {
-      if (scores) *score_at(t, row) = scores[i];
+      if (!keep_scores) {
+        uint64_t* sp = score_at(t, row);
+        *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
+      }
       ++upd;
     }
   }
@@ -905,15 +964,17 @@ namespace {
 uint64_t stage_entries(uint64_t n) { return next_pow2(n * 2 < 64 ? 64 : n * 2); }
 }  // namespace
 
-size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind) {
+size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind, bool lfu) {
   const uint64_t m = stage_entries(n);
   size_t bytes = align256(m * 8) + align256(m * 4) + align256(64);
   if (kind == ScratchKind::kSingleUpsert) bytes += align256(num_buckets);
   if (kind == ScratchKind::kDualUpsert) bytes += align256(n * 4);
+  if (lfu) bytes += align256(m * 8);
   return bytes;
 }
 
-UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind) {
+UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets, ScratchKind kind,
+                                   bool lfu) {
   UpsertScratch s{};
   const uint64_t m = stage_entries(n);
   char* p = static_cast<char*>(base);
@@ -935,6 +996,9 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
   if (kind == ScratchKind::kDualUpsert) {
     s.group = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
   }
+  if (lfu) {
+    s.inc = reinterpret_cast<uint64_t*>(p); p += align256(m * 8);
+  }
   return s;
 }
 
@@ -945,25 +1009,34 @@ cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, S
   if (e == cudaSuccess) e = cudaMemsetAsync(s.cursor, 0, 64, st);
   if (e == cudaSuccess && kind == ScratchKind::kSingleUpsert && s.mark)
     e = cudaMemsetAsync(s.mark, 0, num_buckets, st);
+  if (e == cudaSuccess && s.inc) e = cudaMemsetAsync(s.inc, 0, static_cast<size_t>(s.map_size) * 8, st);
   return e;
 }
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
-                          const uint64_t* keys, const float* values, const uint64_t* scores,
-                          uint64_t step_score, cudaStream_t st, const UpsertExtra& ex) {
+                          const uint64_t* keys, const float* values, const ScoreRule& rule,
+                          cudaStream_t st, const UpsertExtra& ex) {
   if (n == 0) return cudaSuccess;
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
+  const uint64_t* inc_in = rule.lfu() ? rule.in : nullptr;
   if (!t.dual) {
     stage_kernel<<<grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread), kThreads, 0,
-                   st>>>(t, s, n, keys);
-    upsert_single_kernel<<<grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS), kThreads, 0, st>>>(
-        t, s, keys, values, scores, step_score, vec, ex);
+                   st>>>(t, s, n, keys, inc_in);
+    const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
+    if (rule.lfu()) {
+      upsert_single_kernel<true><<<grid, kThreads, 0, st>>>(t, s, keys, values, rule, vec, ex);
+    } else {
+      // one score per call unless the caller gives scores (kCustomized)
+      ScoreRule r = rule;
+      if (rule.policy != kCustomized) r.in = nullptr;
+      if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
+      r.policy = kCustomized;
+      upsert_single_kernel<false><<<grid, kThreads, 0, st>>>(t, s, keys, values, r, vec, ex);
+    }
   } else {
-    dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, t.stats);
-    dual_resident_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, scores,
-                                                                step_score, vec);
-    dual_place_kernel<<<grid_for(n * 32), kThreads, 0, st>>>(t, s, keys, values, scores, step_score,
-                                                             vec);
+    dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, inc_in, t.stats);
+    dual_resident_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, rule, vec);
+    dual_place_kernel<<<grid_for(n * 32), kThreads, 0, st>>>(t, s, keys, values, rule, vec);
     dual_count_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, keys);
     dual_finish_kernel<<<1, 1, 0, st>>>(t, s);
   }
@@ -971,12 +1044,14 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
 }
 
 cudaError_t launch_assign(const TableView& t, const UpsertScratch& s, uint64_t n,
-                          const uint64_t* keys, const float* values, const uint64_t* scores,
-                          cudaStream_t st) {
+                          const uint64_t* keys, const float* values, const ScoreRule& rule,
+                          bool keep_scores, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
-  dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, t.stats);
-  assign_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, scores, vec);
+  dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, rule.lfu() ? rule.in : nullptr,
+                                                         t.stats);
+  assign_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, rule, keep_scores,
+                                                       vec);
   return cudaGetLastError();
 }
 

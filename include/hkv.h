@@ -37,6 +37,30 @@
  * enqueues kernels and returns.  Argument errors are returned at once and
  * enqueue nothing.
  *
+ * Score policies (HKV §3.3 "Scoring policies"; §5 Exp #3c, Table 8 names
+ * kLru, kLfu, kEpochLru, kEpochLfu and kCustomized without defining their
+ * update rules).  A table is created with one policy (mode bits 4-7), which
+ * decides the score a call writes for a key (insert_or_assign,
+ * insert_and_evict, find_or_insert, assign):
+ *   HKV_POLICY_CUSTOMIZED  the caller's score; scores == NULL: the table's
+ *                          step counter, which starts at 1 and grows by 1
+ *                          per NULL-score call (assign with NULL keeps the
+ *                          scores).
+ *   HKV_POLICY_LRU         the table clock: the step counter, which under this
+ *                          policy grows by 1 per score-writing call.  scores
+ *                          must be NULL (else HKV_ERR_INVALID).
+ *   HKV_POLICY_EPOCH_LRU   (epoch << 32) | (clock mod 2^32); scores NULL.
+ *   HKV_POLICY_LFU         a frequency: scores are per-occurrence increments
+ *                          (NULL: 1 each).  The increments of all occurrences
+ *                          of a key in one call add up; a resident key gets
+ *                          old score + sum, an absent key competes with sum;
+ *                          sums saturate at 2^64 - 1.
+ *   HKV_POLICY_EPOCH_LFU   (epoch << 32) | f, where f is the LFU rule applied
+ *                          to the low 32 bits of the old score, saturating at
+ *                          2^32 - 1 (the count survives epoch changes).
+ * The epoch is a 32-bit value of the table (0 at creation, hkv_set_epoch),
+ * read when a call is issued.  find_or_insert never changes a resident key.
+ *
  * Roles (HKV §3.5, Table 4): find, size and export are readers; assign is an
  * updater; insert_or_assign and erase are inserters.  Calls of conflicting
  * roles issued on different streams are ordered by CUDA events in host issue
@@ -61,6 +85,16 @@ enum {
   HKV_MODE_TIERED = 2  /* flag: values above the HBM budget live in mapped host memory (HKV §3.6) */
 };
 
+/* Score policy, ORed into hkv_create's mode (see "Score policies"). */
+enum {
+  HKV_POLICY_CUSTOMIZED = 0x00,
+  HKV_POLICY_LRU = 0x10,
+  HKV_POLICY_LFU = 0x20,
+  HKV_POLICY_EPOCH_LRU = 0x30,
+  HKV_POLICY_EPOCH_LFU = 0x40,
+  HKV_POLICY_MASK = 0xF0
+};
+
 enum {
   HKV_OK = 0,
   HKV_ERR_INVALID = -1,      /* bad argument; nothing was enqueued */
@@ -78,7 +112,8 @@ enum {
  *  capacity        slots; a positive multiple of 128 (B = capacity / 128;
  *                  B >= 2 in dual mode).
  *  dim             float32 elements per value row, >= 1.
- *  mode            HKV_MODE_SINGLE or HKV_MODE_DUAL, optionally | HKV_MODE_TIERED.
+ *  mode            HKV_MODE_SINGLE or HKV_MODE_DUAL, optionally | HKV_MODE_TIERED,
+ *                  | one HKV_POLICY_* (default HKV_POLICY_CUSTOMIZED).
  *  value_hbm_bytes with TIERED: HBM budget for value rows.  Rows of whole
  *                  buckets 0 .. R-1 (R = floor(budget / (128 * 4 * dim)) * 128)
  *                  live in HBM, the rest in mapped pinned host memory.
@@ -108,8 +143,10 @@ hkv_status hkv_find(hkv_table* table, uint64_t n, const uint64_t* keys, float* v
  * bucket is full (dual: both full) it replaces the lowest-ranked entry of the
  * bucket (dual: of the candidate whose lowest rank is lower) if it ranks
  * higher than that entry, else it is rejected.
- *  scores  per-key scores, or NULL: every key of the call gets the table's
- *          step counter, which starts at 1 and grows by 1 per NULL-score call.
+ *  scores  per-key scores (LFU policies: increments) or NULL; the score an
+ *          entry receives follows the table's policy (see "Score
+ *          policies"); under HKV_POLICY_CUSTOMIZED, NULL gives every key of
+ *          the call the step counter.
  * Outcome totals accumulate in hkv_get_op_counts. */
 hkv_status hkv_insert_or_assign(hkv_table* table, uint64_t n, const uint64_t* keys,
                                 const float* values, const uint64_t* scores, void* stream);
@@ -131,7 +168,7 @@ hkv_status hkv_insert_and_evict(hkv_table* table, uint64_t n, const uint64_t* ke
 
 /* Inserter, single-bucket tables only.  HKV §4.1 find_or_insert (lookup
  * with insertion for cold start): absent keys are inserted with their row of
- * values_inout and their score (scores, or the step counter when NULL) under
+ * values_inout and the score the table's policy gives them under
  * HKV Algorithm 2; resident keys are not modified.  Afterwards, for each i:
  * when keys[i] is resident, found_out[i] = 1 and row i of values_inout holds
  * its stored value; otherwise (admission rejected it) found_out[i] = 0 and
@@ -153,9 +190,11 @@ hkv_status hkv_contains(hkv_table* table, uint64_t n, const uint64_t* keys, uint
 hkv_status hkv_find_ptr(hkv_table* table, uint64_t n, const uint64_t* keys, float** values_ptr_out,
                         uint8_t* found_out, uint64_t* scores_out, void* stream);
 
-/* Updater.  HKV §3.5: overwrites the value/* Updater.  HKV §3.5: overwrites the value (and the score when scores !=
- * NULL) of resident keys in place; absent keys are ignored; nothing is
- * inserted, evicted or moved. */
+/* Updater.  HKV §3.5: overwrites the value and the score of resident keys
+ * in place; absent keys are ignored; nothing is inserted, evicted or moved.
+ * The score follows the table's policy (see "Score policies"); under
+ * HKV_POLICY_CUSTOMIZED with scores == NULL the scores are left as they are
+ * and the step counter does not move. */
 hkv_status hkv_assign(hkv_table* table, uint64_t n, const uint64_t* keys, const float* values,
                       const uint64_t* scores, void* stream);
 
@@ -206,6 +245,12 @@ typedef struct hkv_info {
 } hkv_info;
 hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
 
+/* Set the table's 32-bit epoch (HKV §3.3 epoch-aware scoring; see "Score
+ * policies").  Calls issued afterwards use it; calls already issued keep the
+ * epoch they were issued with.  Any policy accepts it; only the EPOCH
+ * policies read it.  Errors: INVALID (NULL table). */
+hkv_status hkv_set_epoch(hkv_table* table, uint32_t epoch);
+
 /* insert_or_assign for callers that cannot let the library allocate.
  *
  * The paper has no counterpart: this is a deployment variant of
@@ -219,11 +264,12 @@ hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
  *  - Limit: the batch's working memory must fit the array, i.e.
  *      a(8M) + a(4M) + 256 + a(B) bytes in single mode and
  *      a(8M) + a(4M) + 256 + a(4n) bytes in dual mode,
- *    with M the smallest power of two >= max(64, 2n), B the bucket count and
- *    a(x) = x rounded up to a multiple of 256.  Larger batches return
- *    HKV_ERR_INVALID and enqueue nothing (split them, or use
- *    hkv_insert_or_assign).  Single mode takes up to 2^20 keys per call for
- *    tables of up to 2^23 buckets.
+ *    plus a(8M) under the LFU policies, with M the smallest power of two
+ *    >= max(64, 2n), B the bucket count and a(x) = x rounded up to a
+ *    multiple of 256.  Larger batches return HKV_ERR_INVALID and enqueue
+ *    nothing (split them, or use hkv_insert_or_assign).  Single mode takes
+ *    up to 2^20 keys per call (2^19 under the LFU policies) for tables of up
+ *    to 2^23 buckets.
  *  - Sharing: every call on every table of a device uses the same array and
  *    clears it before use.  Calls whose kernels overlap on the GPU (on
  *    different streams, from any table) race on it and corrupt each other's
