@@ -22,9 +22,15 @@
 //  R3 the 16 keys 0xFFFFFFFFFFFFFFF0..0xFFFFFFFFFFFFFFFF are reserved
 //     sentinels (EMPTY and LOCKED live there); inputs carrying them are
 //     skipped and counted.
-//  R4 rank of an entry = (score, key), compared lexicographically as
-//     unsigned integers.  Admission and victim choice use the rank, which
-//     breaks the paper's equal-score ties deterministically.
+//  R4 ranks.  HKV Algorithm 2 admits an absent key into a full bucket when
+//     its score is >= the bucket's minimum; Algorithm 3 only when it is >.
+//     Single mode ranks an entry by (score, new, key): `new` marks entries
+//     placed in the bucket by the current call, so an incoming key beats an
+//     older entry of equal score (Algorithm 2's >=), and the key decides
+//     between entries of equal score and age.  The victim is the entry of
+//     lowest rank.  Dual mode ranks by (score, key) (Algorithm 3's >, with
+//     the key as the deterministic tie-break).  Both orders are total, so a
+//     bucket's result never depends on the order of the keys in a batch.
 //  R5 duplicate keys inside one batch collapse to their last occurrence.
 //  R6 within one batch, the unique keys are applied in this serial order:
 //     first every key that is already resident (in-place update, HKV
@@ -98,11 +104,19 @@ bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
     return s1 < s2 || (s1 == s2 && k1 < k2);
 }
 
+// R4, single mode: (score, new, key).
+bool rank_less_new(uint64_t s1, int n1, uint64_t k1, uint64_t s2, int n2, uint64_t k2) {
+    if (s1 != s2) return s1 < s2;
+    if (n1 != n2) return n1 < n2;
+    return k1 < k2;
+}
+
 struct Bucket {
     // Parallel arrays, unordered, size <= kSlots (R9).
     std::vector<uint64_t> keys;
     std::vector<uint64_t> scores;
     std::vector<float> values;   // keys.size() * dim
+    std::vector<uint8_t> fresh;  // 1 = placed by the current call (R4)
 
     int find(uint64_t k) const {
         for (size_t i = 0; i < keys.size(); ++i)
@@ -110,12 +124,17 @@ struct Bucket {
         return -1;
     }
     int size() const { return static_cast<int>(keys.size()); }
-    // Position of the minimum-rank entry (HKV Algorithm 2, arg-min over the
-    // bucket's scores, ties by key per R4).  Bucket must be non-empty.
-    int argmin_rank() const {
+    // Position of the minimum-rank entry (the arg-min over the bucket's
+    // scores of HKV Algorithms 2 and 3, ties per R4: with_new selects the
+    // single-mode rank).  Bucket must be non-empty.
+    int argmin_rank(bool with_new) const {
         int m = 0;
-        for (int i = 1; i < size(); ++i)
-            if (rank_less(scores[i], keys[i], scores[m], keys[m])) m = i;
+        for (int i = 1; i < size(); ++i) {
+            const bool lt = with_new
+                ? rank_less_new(scores[i], fresh[i], keys[i], scores[m], fresh[m], keys[m])
+                : rank_less(scores[i], keys[i], scores[m], keys[m]);
+            if (lt) m = i;
+        }
         return m;
     }
 };
@@ -138,6 +157,7 @@ struct Table {
     uint32_t epoch = 0;                                  // R10
     uint64_t step = 1;                                   // R7
     std::unordered_map<uint64_t, Bucket> buckets;       // created on first use
+    std::vector<uint64_t> placed_in;                    // buckets holding new entries (R4)
     bool filtered = false;
     std::unordered_set<uint64_t> filter;                // single mode only
 
@@ -178,14 +198,19 @@ struct Table {
     void append_entry(Bucket& bk, uint64_t k, uint64_t s, const float* v) {
         bk.keys.push_back(k);
         bk.scores.push_back(s);
+        bk.fresh.push_back(0);
         bk.values.insert(bk.values.end(), v, v + dim);
     }
     void remove_entry(Bucket& bk, int pos) {
         int last = bk.size() - 1;
-        if (pos != last) write_entry(bk, pos, bk.keys[last], bk.scores[last],
-                                     &bk.values[static_cast<size_t>(last) * dim]);
+        if (pos != last) {
+            write_entry(bk, pos, bk.keys[last], bk.scores[last],
+                        &bk.values[static_cast<size_t>(last) * dim]);
+            bk.fresh[pos] = bk.fresh[last];
+        }
         bk.keys.pop_back();
         bk.scores.pop_back();
+        bk.fresh.pop_back();
         bk.values.resize(static_cast<size_t>(last) * dim);
     }
 
@@ -208,14 +233,22 @@ struct Table {
         Bucket& bk = at(b);
         if (bk.size() < kSlots) {                 // first empty slot exists
             append_entry(bk, k, s, v);
+            mark_new(b, bk, bk.size() - 1);
             return kInserted;
         }
-        int m = bk.argmin_rank();                 // bucket full: eviction path
-        if (rank_less(s, k, bk.scores[m], bk.keys[m]))
-            return kRejected;                     // admission control
+        int m = bk.argmin_rank(true);             // bucket full: eviction path
+        // admission control: the incoming key is new to the bucket (R4)
+        if (rank_less_new(s, 1, k, bk.scores[m], bk.fresh[m], bk.keys[m]))
+            return kRejected;
         take_victim(bk, m, victim);
         write_entry(bk, m, k, s, v);              // replace the minimum
+        mark_new(b, bk, m);
         return kEvicted;
+    }
+
+    void mark_new(uint64_t b, Bucket& bk, int pos) {
+        bk.fresh[pos] = 1;
+        placed_in.push_back(b);
     }
 
     // HKV Algorithm 3 (score-based dual-bucket upsert), for an absent key.
@@ -228,7 +261,7 @@ struct Table {
             append_entry(target, k, s, v);
             return kInserted;
         }
-        int m1 = x.argmin_rank(), m2 = y.argmin_rank();      // phase D2
+        int m1 = x.argmin_rank(false), m2 = y.argmin_rank(false);  // phase D2
         bool pick2 = rank_less(y.scores[m2], y.keys[m2], x.scores[m1], x.keys[m1]);
         Bucket& bs = pick2 ? y : x;
         int m = pick2 ? m2 : m1;
@@ -353,6 +386,11 @@ struct Table {
                 }
             }
         }
+        for (uint64_t b : placed_in) {            // R4: "new" lasts one call
+            Bucket& bk = at(b);
+            std::fill(bk.fresh.begin(), bk.fresh.end(), 0);
+        }
+        placed_in.clear();
         c.admitted = admitted.size();
         c.rejected = absent.size() - admitted.size();
         return c;

@@ -7,7 +7,9 @@ different form:
   under the batch reading "resident keys update first, then absent keys":
   after a call, bucket b holds the 128 highest-ranked of (its residents after
   the in-place updates) plus (the absent keys hashed to it); rank = (score,
-  key).  No slot, no arg-min loop, no eviction step.
+  key is new to the table in this call, key) -- an incoming key beats an
+  older entry of equal score, as Algorithm 2 admits on score >= minimum.
+  No slot, no arg-min loop, no eviction step.
 * dual-bucket mode replays HierarchicalKV §3.4 (Algorithm 3) key by key on
   Python dicts.
 * score policies (kLru, kLfu, kEpochLru, kEpochLfu, kCustomized; HKV §3.3 and
@@ -126,12 +128,14 @@ class BruteTable:
             for i in absent:
                 self._dual_insert(keys[i], score(i, keys[i], None), tuple(values[i].tolist()))
         else:
+            new = {keys[i] for i in absent}
             for i in absent:
                 k = keys[i]
                 self.bk[self.b1(k)][k] = (score(i, k, None), tuple(values[i].tolist()))
             for b, d in self.bk.items():
                 if len(d) > SLOTS:
-                    top = sorted(d.items(), key=lambda kv: (kv[1][0], kv[0]), reverse=True)[:SLOTS]
+                    top = sorted(d.items(), key=lambda kv: (kv[1][0], kv[0] in new, kv[0]),
+                                 reverse=True)[:SLOTS]
                     self.bk[b] = dict(top)
         after = self.residents()
         if evicted_out is not None:

@@ -209,6 +209,45 @@ def test_step_scores(oracle_mod):
     assert t.step == 4
 
 
+def test_alg2_admits_on_equal_score(oracle_mod):
+    """HKV Algorithm 2 admits an incoming key whose score equals the bucket
+    minimum (score >= min) and evicts the minimum; ties among older entries,
+    and among the call's own new entries, go by key.  Hand-worked on one
+    bucket (dim 1, value = key)."""
+    t = oracle_mod.OracleTable(1, 1)
+
+    def put(keys, score):
+        k = np.array(keys, np.uint64)
+        return t.insert_or_assign(k, k.astype(np.float32), np.full(k.size, score, np.uint64))
+
+    def keys():
+        return sorted(t.export()[0].tolist())
+
+    put(range(1000, 1128), 5)                       # full, every score 5
+    c = put([7], 5)                                 # 5 >= 5: admitted, evicts key 1000
+    assert c["admitted"] == 1 and c["evicted"] == 1
+    assert keys() == [7] + list(range(1001, 1128))
+    c = put([3], 4)                                 # 4 < 5: rejected
+    assert c["rejected"] == 1 and keys() == [7] + list(range(1001, 1128))
+    c = put([9, 2], 5)                              # two new keys; 7 is now old
+    assert c["admitted"] == 2 and c["evicted"] == 2
+    assert keys() == [2, 9] + list(range(1002, 1128))
+    t.erase(np.array([1002], np.uint64))            # one free slot
+    c = put([30, 20], 5)                            # free slot, then evicts old key 2
+    assert c["admitted"] == 2 and c["evicted"] == 1
+    assert keys() == [9, 20, 30] + list(range(1003, 1128))
+    # new keys of one call compete by key: 127 entries of score 9, one old
+    # entry of score 5, two new keys of score 5 -> the larger new key stays
+    t2 = oracle_mod.OracleTable(1, 1)
+    k = np.arange(2000, 2127, dtype=np.uint64)
+    t2.insert_or_assign(k, k.astype(np.float32), np.full(k.size, 9, np.uint64))
+    t2.insert_or_assign(np.array([11], np.uint64), np.ones(1, np.float32), np.array([5], np.uint64))
+    c = t2.insert_or_assign(np.array([50, 40], np.uint64), np.ones(2, np.float32),
+                            np.array([5, 5], np.uint64))
+    assert c["admitted"] == 1 and c["rejected"] == 1 and c["evicted"] == 1
+    assert sorted(t2.export()[0].tolist()) == [50] + list(range(2000, 2127))
+
+
 # --------------------------------------------------------------------------
 # Paper special cases and statistics.
 # --------------------------------------------------------------------------
