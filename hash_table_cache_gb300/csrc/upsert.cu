@@ -16,7 +16,7 @@
 //      memory, scans its stage run 32 positions at a time, applies the
 //      in-place updates of resident keys, then places the absent keys: the
 //      free slots in slot order first, then, for each remaining absent key, a
-//      warp arg-min over the rank (score, key) decides admission and the
+//      warp arg-min over the rank (score, new, key) decides admission and the
 //      victim.  Keys, scores and digests are written back once per bucket and
 //      the value rows of the final occupants are copied by 8-lane tiles.
 // With one owner per bucket there is no slot locking and no retry; the result
@@ -190,9 +190,21 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
   warp_add(&t.stats->reserved, reserved);
 }
 
-// Rank order (HKV Algorithm 2 arg-min, ties by key): true when (s1,k1) < (s2,k2).
+// Rank order of dual mode (HKV Algorithm 3 arg-min and its strict admission,
+// ties by key): true when (s1,k1) < (s2,k2).
 __device__ __forceinline__ bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
   return s1 < s2 || (s1 == s2 && k1 < k2);
+}
+
+// Rank order of single mode: (score, new, key), where `new` marks an entry
+// placed in the bucket by the current call.  HKV Algorithm 2 admits an absent
+// key when its score is >= the bucket minimum, so an incoming key outranks an
+// older entry of equal score; the key orders entries of equal score and age.
+__device__ __forceinline__ bool rank3_less(uint64_t s1, uint32_t n1, uint64_t k1, uint64_t s2,
+                                           uint32_t n2, uint64_t k2) {
+  if (s1 != s2) return s1 < s2;
+  if (n1 != n2) return n1 < n2;
+  return k1 < k2;
 }
 
 // ---------------------------------------------------------------------------
@@ -404,60 +416,66 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       const uint32_t E = __popc(em);
       __syncwarp();
       // The lane's four bucket entries sorted by rank (five compare-exchanges).
+      // An entry's `new` bit is its fresh mark; every pending key is new.
       uint64_t rs[4], rk[4];
-      uint32_t rq[4];
+      uint32_t rq[4], rn[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         rs[q] = st.score[lane * 4 + q];
         rk[q] = st.key[lane * 4 + q];
         rq[q] = lane * 4 + q;
+        rn[q] = (st.fresh[lane >> 3] >> ((lane * 4 + q) & 31)) & 1u;
       }
       auto cx = [&](int x, int y) {
-        if (rank_less(rs[y], rk[y], rs[x], rk[x])) {
+        if (rank3_less(rs[y], rn[y], rk[y], rs[x], rn[x], rk[x])) {
           const uint64_t ts = rs[x], tk = rk[x];
-          const uint32_t tq = rq[x];
-          rs[x] = rs[y]; rk[x] = rk[y]; rq[x] = rq[y];
-          rs[y] = ts; rk[y] = tk; rq[y] = tq;
+          const uint32_t tq = rq[x], tn = rn[x];
+          rs[x] = rs[y]; rk[x] = rk[y]; rq[x] = rq[y]; rn[x] = rn[y];
+          rs[y] = ts; rk[y] = tk; rq[y] = tq; rn[y] = tn;
         }
       };
       cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
       // 32-bit keys that preserve the rank order (ties allowed): the score
-      // relative to the union's minimum, with the top 16 key bits appended
-      // when the scores span less than 2^16, shifted right when they span
-      // more than 2^32.  Each extraction is then one 32-bit warp reduction;
-      // lanes tied on it are resolved exactly.
+      // relative to the union's minimum, with the new bit and the top 16 key
+      // bits appended when the scores span less than 2^15, shifted right when
+      // they span more than 2^32.  Each extraction is then one 32-bit warp
+      // reduction; lanes tied on it are resolved exactly.
       unsigned sel;
-      const uint64_t smin = warp_min_u64(pending && rank_less(se, ke, rs[0], rk[0]) ? se : rs[0],
-                                         true, sel);
+      const uint64_t smin = warp_min_u64(pending && se < rs[0] ? se : rs[0], true, sel);
       const uint64_t smax = ~warp_min_u64(~((pending && se > rs[3]) ? se : rs[3]), true, sel);
       const uint64_t span = smax - smin;
       const int sh = span >> 32 ? 32 - __clzll(static_cast<long long>(span)) : 0;
-      auto fkey = [&](uint64_t sc, uint64_t k) -> uint32_t {
-        if (span < 65536) return static_cast<uint32_t>(((sc - smin) << 16) | (k >> 48));
+      auto fkey = [&](uint64_t sc, uint32_t nw, uint64_t k) -> uint32_t {
+        if (span < 32768)
+          return static_cast<uint32_t>(((sc - smin) << 17) | (static_cast<uint64_t>(nw) << 16) |
+                                       (k >> 48));
         return static_cast<uint32_t>((sc - smin) >> sh);
       };
       uint32_t rf[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) rf[q] = fkey(rs[q], rk[q]);
-      const uint32_t mf = pending ? fkey(se, ke) : 0xFFFFFFFFu;
+      for (int q = 0; q < 4; ++q) rf[q] = fkey(rs[q], rn[q], rk[q]);
+      const uint32_t mf = pending ? fkey(se, 1u, ke) : 0xFFFFFFFFu;
       int head = 0;
       for (uint32_t x = 0; x < E; ++x) {
-        uint32_t hf = 0xFFFFFFFFu;
+        uint32_t hf = 0xFFFFFFFFu, hn = 1u;
         uint64_t hs = ~0ull, hk = ~0ull;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q == head) { hf = rf[q]; hs = rs[q]; hk = rk[q]; }
+          if (q == head) { hf = rf[q]; hs = rs[q]; hk = rk[q]; hn = rn[q]; }
         const bool take_miss =
-            pending && (mf < hf || (mf == hf && rank_less(se, ke, hs, hk)));
+            pending && (mf < hf || (mf == hf && rank3_less(se, 1u, ke, hs, hn, hk)));
         const uint32_t lf = take_miss ? mf : hf;
         const uint32_t m = __reduce_min_sync(0xFFFFFFFFu, lf);
         const unsigned tied = __ballot_sync(0xFFFFFFFFu, lf == m);
         unsigned wl = __ffs(tied) - 1;
         if (tied & (tied - 1)) {  // several lanes share the 32-bit key: exact rank
           const uint64_t cs = take_miss ? se : hs, ck = take_miss ? ke : hk;
+          const uint32_t cn = take_miss ? 1u : hn;
           unsigned sel_s, sel_k;
           warp_min_u64(cs, (tied >> lane) & 1u, sel_s);
-          warp_min_u64(ck, (sel_s >> lane) & 1u, sel_k);
+          const unsigned old_s = __ballot_sync(0xFFFFFFFFu, ((sel_s >> lane) & 1u) && cn == 0u);
+          const unsigned sel_n = old_s ? old_s : sel_s;
+          warp_min_u64(ck, (sel_n >> lane) & 1u, sel_k);
           wl = __ffs(sel_k) - 1;
         }
         if (lane == wl) {
