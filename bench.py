@@ -256,6 +256,8 @@ def run_gpu(args):
     t.reset_op_counts()
     with Clocks(local) as clk:
         w0 = time.time()
+        # NVTX range "timed": lets a profiler select the timed launches
+        torch.cuda.nvtx.range_push("timed")
         for s in range(args.warmup, nsteps):
             flush.zero_()
             e0, e1, e2 = ev[s]
@@ -264,6 +266,7 @@ def run_gpu(args):
             e1.record(stream)
             t.find(fq[s], vout, fout, sout)
             e2.record(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         clk.mark(w0, time.time())
     if world > 1:
@@ -317,7 +320,7 @@ def run_gpu(args):
          for s in range(3)]) / 1e9
     fio_v = [qv.clone() for _ in range(3)]
     api["find_or_insert_bkvs"] = BATCH / statistics.median(
-        [timed(lambda: t.find_or_insert(up_k[s + 3], fio_v[s], None)) for s in range(3)]) / 1e9
+        [timed(lambda: t.find_or_insert(up_k[(s + 3) % nsteps], fio_v[s], None)) for s in range(3)]) / 1e9
 
     # End to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, runs insert_or_assign + find and

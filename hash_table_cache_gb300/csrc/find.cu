@@ -6,10 +6,11 @@
 // the bucket's 128-byte digest line, so the tile reads the line with a single
 // coalesced request; the byte compare is a SWAR zero-byte test (the role of
 // the paper's 32 x __vcmpeq4).  A lane whose bytes match confirms the key
-// with one 8-byte load; a tile ballot picks the hit.  The same 8 lanes then
+// with one 16-byte (key, score) load; a tile ballot picks the hit.  The same 8 lanes then
 // move the value row in 16-byte vectors (one 128-byte row per instruction)
 // with streaming stores.  The grid is a multiple of the SM count and each
-// tile walks keys with a grid stride, prefetching its next key.
+// tile walks keys with a grid stride, loading its next keys one iteration
+// ahead.
 #include "launch.h"
 
 namespace hkv {
@@ -25,12 +26,15 @@ namespace {
 constexpr int kFindKeysPerTile = HKV_FIND_KEYS_PER_TILE;
 
 // Probe for U keys at once: the U digest-line loads, then the U first-match
-// key loads, are issued back to back so a tile keeps U requests in flight.
+// (key, score) pair loads, are issued back to back so a tile keeps U requests
+// in flight.  Returns the slot (or -1) and, on a hit, the score, which comes
+// with the key in the same 16-byte load.
 template <int U>
 __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64_t (&b)[U],
                                                 const uint64_t (&k)[U], const uint32_t (&pat)[U],
                                                 const bool (&act)[U], unsigned sub, unsigned tmask,
-                                                int (&slot)[U]) {
+                                                int (&slot)[U],
+                                                uint64_t (&score)[U]) {
   uint4 dg[U];
 #pragma unroll
   for (int u = 0; u < U; ++u)
@@ -43,25 +47,34 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
       m[u] = byte_match4(dg[u].x, pat[u]) | (byte_match4(dg[u].y, pat[u]) << 4) |
              (byte_match4(dg[u].z, pat[u]) << 8) | (byte_match4(dg[u].w, pat[u]) << 12);
   }
-  uint64_t kk[U];
+  ulonglong2 kk[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u)
-    if (m[u]) kk[u] = ld_nc_u64(key_at(t, b[u] * kSlots + sub * 16 + (__ffs(m[u]) - 1)));
+  for (int u = 0; u < U; ++u) {
+    if (m[u]) {
+      const uint64_t row = b[u] * kSlots + sub * 16 + (__ffs(m[u]) - 1);
+      kk[u] = ld_nc_pair(key_at(t, row));
+    }
+  }
   int hit[U];
+  uint64_t hs[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     hit[u] = -1;
+    hs[u] = 0;
     if (m[u]) {
       int bit = __ffs(m[u]) - 1;
-      if (kk[u] == k[u]) {
+      if (kk[u].x == k[u]) {
         hit[u] = static_cast<int>(sub * 16 + bit);
+        hs[u] = kk[u].y;
       } else {
         m[u] &= m[u] - 1;
         while (m[u]) {  // further digest matches (rare)
           bit = __ffs(m[u]) - 1;
           m[u] &= m[u] - 1;
-          if (ld_nc_u64(key_at(t, b[u] * kSlots + sub * 16 + bit)) == k[u]) {
+          const ulonglong2 p = ld_nc_pair(key_at(t, b[u] * kSlots + sub * 16 + bit));
+          if (p.x == k[u]) {
             hit[u] = static_cast<int>(sub * 16 + bit);
+            hs[u] = p.y;
             break;
           }
         }
@@ -71,7 +84,9 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
-    slot[u] = bal ? __shfl_sync(tmask, hit[u], __ffs(bal) - 1) : -1;
+    const int lead = bal ? __ffs(bal) - 1 : static_cast<int>(lane_id());
+    slot[u] = bal ? __shfl_sync(tmask, hit[u], lead) : -1;
+    score[u] = __shfl_sync(tmask, hs[u], lead);
   }
 }
 
@@ -79,7 +94,8 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
 enum FindOut { kOutValues = 0, kOutNone = 1, kOutPointer = 2 };
 
 // One 8-lane tile handles U keys per iteration: keys i, i+T, ..., i+(U-1)T
-// for T tiles in the grid.
+// for T tiles in the grid; the next iteration's keys are loaded at the top
+// of the current one.
 template <bool kDual, int U, int kOut>
 __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
     find_kernel(TableView t, uint64_t n, const uint64_t* keys, float* values_out,
@@ -89,15 +105,22 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
   const unsigned tmask = 0xFFu << (lane & 24u);
   const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
   unsigned long long reserved = 0;
-  for (uint64_t i0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i0 < n;
-       i0 += tiles * U) {
+  uint64_t i0 = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+  uint64_t kn[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint64_t i = i0 + u * tiles;
+    kn[u] = i < n ? keys[i] : kEmptyKey;
+  }
+  for (; i0 < n; i0 += tiles * U) {
     uint64_t k[U], b[U];
     uint32_t pat[U];
     bool act[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint64_t i = i0 + u * tiles;
-      k[u] = i < n ? keys[i] : kEmptyKey;
+      k[u] = kn[u];
+      const uint64_t i = i0 + (U + u) * tiles;
+      kn[u] = i < n ? keys[i] : kEmptyKey;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -109,13 +132,15 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
       b[u] = bucket_of_hash(t, h);
     }
     int slot[U];
-    tile_probe_many<U>(t, b, k, pat, act, sub, tmask, slot);
+    uint64_t sc[U];
+    tile_probe_many<U>(t, b, k, pat, act, sub, tmask, slot, sc);
     if (kDual) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (act[u] && slot[u] < 0) {
           b[u] = bucket2_of(t, k[u], b[u]);
           slot[u] = tile_probe<true>(t, b[u], k[u], pat[u], sub, tmask);
+          if (slot[u] >= 0) sc[u] = ld_nc_u64(score_at(t, b[u] * kSlots + slot[u]));
         }
       }
     }
@@ -140,7 +165,7 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
         found_out[i] = slot[u] >= 0 ? 1 : 0;
         const uint64_t row = b[u] * kSlots + static_cast<uint64_t>(slot[u]);
         if (kOut == kOutPointer) ptrs_out[i] = slot[u] >= 0 ? row_ptr(t, row) : nullptr;
-        if (slot[u] >= 0 && scores_out) scores_out[i] = *score_at(t, row);
+        if (slot[u] >= 0 && scores_out) scores_out[i] = sc[u];
       }
     }
   }

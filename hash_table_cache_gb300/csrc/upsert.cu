@@ -39,6 +39,9 @@ constexpr int kThreads = 256;
 #ifndef HKV_UPSERT_MIN_BLOCKS
 #define HKV_UPSERT_MIN_BLOCKS 3
 #endif
+#ifndef HKV_UPSERT_PREFETCH
+#define HKV_UPSERT_PREFETCH 1
+#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 constexpr int kSpinLimit = 1 << 20;
 
@@ -271,6 +274,65 @@ __device__ __forceinline__ uint64_t warp_min_u64(uint64_t v, bool valid, unsigne
   return (static_cast<uint64_t>(mh) << 32) | ml;
 }
 
+// Exact form of the E extractions of phase B (below), for a bucket whose
+// 31-bit rank keys tie at the front: each extraction takes the warp's
+// minimum 31-bit key, and among the elements that share it the lowest exact
+// rank (score, new, key), first within the lane, then across the warp.
+// f0..f3 are the lane's entries' keys, mf its pending key's (0xFFFFFFFF: no
+// pending key).  Returns the lane's extracted entries (bits 0..3) and whether
+// its pending key survived.  Kept out of line: it runs rarely.
+struct ExactOut {
+  uint32_t rem;
+  bool pending;
+};
+
+template <class Stage>
+__device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, uint32_t E,
+                                               uint32_t f0, uint32_t f1, uint32_t f2, uint32_t f3,
+                                               uint32_t mf, bool pending, uint64_t se,
+                                               uint64_t ke) {
+  constexpr uint32_t kGone = 0xFFFFFFFFu;
+  uint32_t rf[4] = {f0, f1, f2, f3};
+  const uint32_t fw = st->fresh[lane >> 3] >> ((lane * 4) & 31);
+  uint32_t rem = 0;
+  for (uint32_t x = 0; x < E; ++x) {
+    const uint32_t lf = min(min(min(rf[0], rf[1]), min(rf[2], rf[3])), mf);
+    const uint32_t m = __reduce_min_sync(0xFFFFFFFFu, lf);
+    const uint32_t eq = (rf[0] == m ? 1u : 0u) | (rf[1] == m ? 2u : 0u) |
+                        (rf[2] == m ? 4u : 0u) | (rf[3] == m ? 8u : 0u) | (mf == m ? 16u : 0u);
+    uint64_t bs = ~0ull, bk = ~0ull;
+    uint32_t bn = 1u, bbit = 0;
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      if (!((eq >> q) & 1u)) continue;
+      const uint64_t cs = q < 4 ? st->score[lane * 4 + q] : se;
+      const uint64_t ck = q < 4 ? st->key[lane * 4 + q] : ke;
+      const uint32_t cn = q < 4 ? (fw >> q) & 1u : 1u;
+      if (!bbit || rank3_less(cs, cn, ck, bs, bn, bk)) {
+        bs = cs;
+        bk = ck;
+        bn = cn;
+        bbit = 1u << q;
+      }
+    }
+    unsigned sel_s, sel_k;
+    warp_min_u64(bs, bbit != 0, sel_s);
+    const unsigned old_s = __ballot_sync(0xFFFFFFFFu, ((sel_s >> lane) & 1u) && bn == 0u);
+    const unsigned sel_n = old_s ? old_s : sel_s;
+    warp_min_u64(bk, (sel_n >> lane) & 1u, sel_k);
+    const uint32_t take = lane == static_cast<unsigned>(__ffs(sel_k) - 1) ? bbit : 0u;
+    if (take & 16u) {
+      pending = false;  // rejected
+      mf = kGone;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (take & (1u << q)) rf[q] = kGone;
+    rem |= take & 15u;
+  }
+  return {rem, pending};
+}
+
 // kLfu: the table sums increments (kLfu, kEpochLfu).  Otherwise every key of
 // the call gets rule.in[e] or the constant rule.clock (the host folds the
 // clock policies into that constant).
@@ -296,6 +358,13 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
        b += nwarps) {
     if (scr.mark && !scr.mark[b]) continue;  // no key of the batch here
     const uint64_t base = b * kSlots + lane * 4;
+    // The warp's next bucket: its key/score pairs and digest line go to L2
+    // now, so the loads at the top of the next iteration do not wait on DRAM.
+    if (HKV_UPSERT_PREFETCH && lane == 0 && b + nwarps < nb &&
+        (!scr.mark || scr.mark[b + nwarps])) {
+      prefetch_l2_bulk(key_at(t, (b + nwarps) * kSlots), kSlots * 16);
+      prefetch_l2_bulk(t.digests + (b + nwarps) * kSlots, kSlots);
+    }
     // This bucket's stage run: from lo, past a_end, up to the first free
     // position at or after a_end (linear probing leaves no gap in a run).
     const uint64_t lo = area_start(b, S, nb, scr.area_shift);
@@ -389,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     // keys.  For the E absent keys left, applying Algorithm 2 to each in turn
     // leaves the 128 highest ranks of (bucket entries + those keys), so the
     // warp drops the E lowest-ranked of that union directly: E extractions of
-    // the union's minimum, each one warp arg-min over per-lane candidates (the
-    // lane's lowest remaining bucket entry, presorted, or its own absent key).
-    // Extracted absent keys are rejected; the absent keys left take the slots
-    // of the extracted entries.
+    // the union's minimum, each one 32-bit warp reduction over the lanes'
+    // candidates (its four bucket entries and its own absent key).  Extracted
+    // absent keys are rejected; the absent keys left take the slots of the
+    // extracted entries.
     uint32_t nfree = 0, used = 0;
     auto phase_b = [&](uint32_t e, uint64_t ke, bool miss, uint64_t inc) {
       const uint64_t se = miss ? score_of(e, inc, false, 0) : 0;
@@ -415,84 +484,76 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       if (!em) return;
       const uint32_t E = __popc(em);
       __syncwarp();
-      // The lane's four bucket entries sorted by rank (five compare-exchanges).
-      // An entry's `new` bit is its fresh mark; every pending key is new.
-      uint64_t rs[4], rk[4];
-      uint32_t rq[4], rn[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        rs[q] = st.score[lane * 4 + q];
-        rk[q] = st.key[lane * 4 + q];
-        rq[q] = lane * 4 + q;
-        rn[q] = (st.fresh[lane >> 3] >> ((lane * 4 + q) & 31)) & 1u;
-      }
-      auto cx = [&](int x, int y) {
-        if (rank3_less(rs[y], rn[y], rk[y], rs[x], rn[x], rk[x])) {
-          const uint64_t ts = rs[x], tk = rk[x];
-          const uint32_t tq = rq[x], tn = rn[x];
-          rs[x] = rs[y]; rk[x] = rk[y]; rq[x] = rq[y]; rn[x] = rn[y];
-          rs[y] = ts; rk[y] = tk; rq[y] = tq; rn[y] = tn;
-        }
-      };
-      cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
-      // 32-bit keys that preserve the rank order (ties allowed): the score
+      // 31-bit keys that preserve the rank order (ties allowed): the score
       // relative to the union's minimum, with the new bit and the top 16 key
-      // bits appended when the scores span less than 2^15, shifted right when
-      // they span more than 2^32.  Each extraction is then one 32-bit warp
-      // reduction; lanes tied on it are resolved exactly.
+      // bits appended when the scores span less than 2^14, shifted right to
+      // 31 bits when they span more than 2^31.  0xFFFFFFFF marks an element
+      // that is no longer a candidate.  An entry's `new` bit is its fresh
+      // mark; every pending key is new.
+      constexpr uint32_t kGone = 0xFFFFFFFFu;
+      uint64_t s4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s4[q] = st.score[lane * 4 + q];
+      const uint32_t fw = st.fresh[lane >> 3] >> ((lane * 4) & 31);  // the lane's 4 fresh bits
+      uint64_t lo_s = min(min(s4[0], s4[1]), min(s4[2], s4[3]));
+      uint64_t hi_s = max(max(s4[0], s4[1]), max(s4[2], s4[3]));
+      if (pending) {
+        lo_s = min(lo_s, se);
+        hi_s = max(hi_s, se);
+      }
       unsigned sel;
-      const uint64_t smin = warp_min_u64(pending && se < rs[0] ? se : rs[0], true, sel);
-      const uint64_t smax = ~warp_min_u64(~((pending && se > rs[3]) ? se : rs[3]), true, sel);
+      const uint64_t smin = warp_min_u64(lo_s, true, sel);
+      const uint64_t smax = ~warp_min_u64(~hi_s, true, sel);
       const uint64_t span = smax - smin;
-      const int sh = span >> 32 ? 32 - __clzll(static_cast<long long>(span)) : 0;
+      const int nbits = span ? 64 - __clzll(static_cast<long long>(span)) : 0;
+      const int sh = nbits > 31 ? nbits - 31 : 0;
       auto fkey = [&](uint64_t sc, uint32_t nw, uint64_t k) -> uint32_t {
-        if (span < 32768)
+        if (span < 16384)
           return static_cast<uint32_t>(((sc - smin) << 17) | (static_cast<uint64_t>(nw) << 16) |
                                        (k >> 48));
         return static_cast<uint32_t>((sc - smin) >> sh);
       };
       uint32_t rf[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) rf[q] = fkey(rs[q], rn[q], rk[q]);
-      const uint32_t mf = pending ? fkey(se, 1u, ke) : 0xFFFFFFFFu;
-      int head = 0;
+      for (int q = 0; q < 4; ++q) rf[q] = fkey(s4[q], (fw >> q) & 1u, st.key[lane * 4 + q]);
+      const uint32_t mf0 = pending ? fkey(se, 1u, ke) : kGone;
+      const bool pending0 = pending;
+      uint32_t mf = mf0;
+      // E extractions of the union's minimum.  Fast pass: every element equal
+      // to the warp minimum leaves; when the 31-bit keys of the extracted
+      // elements are distinct that is exactly one element per extraction,
+      // which the count at the end confirms.
+      uint32_t rem = 0;  // the lane's bucket entries taken out
+#pragma unroll 1
       for (uint32_t x = 0; x < E; ++x) {
-        uint32_t hf = 0xFFFFFFFFu, hn = 1u;
-        uint64_t hs = ~0ull, hk = ~0ull;
+        const uint32_t m =
+            __reduce_min_sync(0xFFFFFFFFu, min(min(min(rf[0], rf[1]), min(rf[2], rf[3])), mf));
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q == head) { hf = rf[q]; hs = rs[q]; hk = rk[q]; hn = rn[q]; }
-        const bool take_miss =
-            pending && (mf < hf || (mf == hf && rank3_less(se, 1u, ke, hs, hn, hk)));
-        const uint32_t lf = take_miss ? mf : hf;
-        const uint32_t m = __reduce_min_sync(0xFFFFFFFFu, lf);
-        const unsigned tied = __ballot_sync(0xFFFFFFFFu, lf == m);
-        unsigned wl = __ffs(tied) - 1;
-        if (tied & (tied - 1)) {  // several lanes share the 32-bit key: exact rank
-          const uint64_t cs = take_miss ? se : hs, ck = take_miss ? ke : hk;
-          const uint32_t cn = take_miss ? 1u : hn;
-          unsigned sel_s, sel_k;
-          warp_min_u64(cs, (tied >> lane) & 1u, sel_s);
-          const unsigned old_s = __ballot_sync(0xFFFFFFFFu, ((sel_s >> lane) & 1u) && cn == 0u);
-          const unsigned sel_n = old_s ? old_s : sel_s;
-          warp_min_u64(ck, (sel_n >> lane) & 1u, sel_k);
-          wl = __ffs(sel_k) - 1;
-        }
-        if (lane == wl) {
-          if (take_miss) pending = false;  // rejected
-          else ++head;                      // that entry leaves the bucket
-        }
+          if (rf[q] == m) { rf[q] = kGone; rem |= 1u << q; }
+        if (mf == m) { mf = kGone; pending = false; }
       }
-      // The lane's extracted entries are its first `head` sorted slots.
+      const uint32_t out = __popc(rem) + ((pending0 && !pending) ? 1u : 0u);
+      if (__reduce_add_sync(0xFFFFFFFFu, out) != E) {
+        // Equal 31-bit keys met at the front: redo with exact ranks.
+        const ExactOut r = extract_exact(
+            &st, lane, E, fkey(s4[0], fw & 1u, st.key[lane * 4]),
+            fkey(s4[1], (fw >> 1) & 1u, st.key[lane * 4 + 1]),
+            fkey(s4[2], (fw >> 2) & 1u, st.key[lane * 4 + 2]),
+            fkey(s4[3], (fw >> 3) & 1u, st.key[lane * 4 + 3]), mf0, pending0, se, ke);
+        rem = r.rem;
+        pending = r.pending;
+      }
+      // Extracted bucket entries: list them in slot order for the pending keys.
       uint32_t n_ext;
-      uint32_t pos = prefix_small(static_cast<uint32_t>(head), n_ext);
+      uint32_t pos = prefix_small(static_cast<uint32_t>(__popc(rem)), n_ext);
       uint32_t ev = 0, fr = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        if (q < head) {
-          const uint32_t slot = rq[q];
+        if (rem & (1u << q)) {
+          const uint32_t slot = lane * 4 + q;
           st.list[pos++] = static_cast<uint8_t>(slot);
-          if (st.fresh[slot >> 5] & (1u << (slot & 31))) {
+          if ((fw >> q) & 1u) {
             ++fr;  // admitted earlier this call
           } else {
             ++ev;  // pre-call resident
@@ -558,6 +619,9 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
           if (kLfu) st.einc[p] = scr.inc[(lo + 32ull * w + lane) & smask];
         }
         ne += __popc(m);
+        // the entry's input value row is read in phase C: start it now
+        if (HKV_UPSERT_PREFETCH && vec && we[w] != kNone)
+          prefetch_l2_bulk(values_in + static_cast<uint64_t>(we[w]) * t.dim, t.dim * 4);
       }
       __syncwarp();
       // (loops kept rolled: one copy of each phase keeps the code in cache)
