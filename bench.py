@@ -63,6 +63,71 @@ def upsert_bytes(n_keys, dim, n_buckets_touched, n_rows_written, with_scores):
             + n_rows_written * (16 + d))
 
 
+def probe_access_rates(dim):
+    """Random-read rates of this GPU (reads/s) for 32-byte sectors, 128-byte
+    lines and value rows of 4*dim bytes, measured by libhkv_probe.so over a
+    2 GiB buffer (see csrc/access_probe.cu)."""
+    import ctypes
+    from hash_table_cache_gb300 import _build
+    lib = ctypes.CDLL(_build.PROBE_LIB)
+    lib.hkv_probe_random_reads.argtypes = [ctypes.c_uint32, ctypes.c_uint64,
+                                           ctypes.POINTER(ctypes.c_double)]
+    lib.hkv_probe_random_reads.restype = ctypes.c_int
+    rates = {}
+    for g in sorted({32, 128, 4 * dim}):
+        r = ctypes.c_double(0.0)
+        st = lib.hkv_probe_random_reads(g, 2 << 30, ctypes.byref(r))
+        rates[g] = r.value if st == 0 else None
+    return rates
+
+
+def find_access_floor(n, dim, hit, num_buckets, rates, hbm_gbs):
+    """Lower bound on one find batch from the measured random-read rates: per
+    key the key/score sectors of the digest matches (1 + 127/256 on a hit,
+    128/256 on a miss) and, on a hit, the value row; one digest line per
+    touched bucket; the input keys, output rows, scores and flags streamed at
+    the copy bandwidth.  The terms are added (no overlap assumed)."""
+    import math
+    sectors = n * (hit * (1 + 127 / 256) + (1 - hit) * 128 / 256)
+    rows = n * hit
+    lines = num_buckets * (1 - math.exp(-n / num_buckets))
+    seq = n * (8 + hit * (4 * dim + 8) + 1)
+    return sectors / rates[32] + rows / rates[4 * dim] + lines / rates[128] + seq / (hbm_gbs * 1e9)
+
+
+def upsert_access_floor(n, dim, rows_written, buckets_touched, rates, hbm_gbs):
+    """Lower bound on one single-bucket insert_or_assign call from the measured
+    random-read rates: per written row one random read of the input row, one
+    random write of the table row (costed as a read) and one key/score sector
+    write; per touched bucket its 2 KiB of key/score pairs and its digest line
+    read and written, plus the input keys, streamed at the copy bandwidth."""
+    seq = buckets_touched * (2048 + 256) + 8 * n
+    return (2 * rows_written / rates[4 * dim] + rows_written / rates[32]
+            + seq / (hbm_gbs * 1e9))
+
+
+# DRAM bytes (read + write) of one launch, from an ncu capture of the timed
+# region of `python bench.py --skip-sweep --no-cpu-baseline --steps 3
+# --warmup 3` (profiles/find_kernel_c2.md), valid only while the kernel's
+# sources are the ones captured (sha256 prefix over the listed files).
+NCU_TRAFFIC = {
+    "find_kernel": {"bytes": 164763648 + 69147136, "sources": ("find.cu", "common.cuh", "launch.h"),
+                    "sha256": "b8d4766bd92480c0"},
+}
+
+
+def ncu_traffic(kernel):
+    import hashlib
+    rec = NCU_TRAFFIC.get(kernel)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, "hash_table_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["sha256"] else None
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -292,13 +357,25 @@ def run_gpu(args):
     rows = (counts["updated"] + counts["admitted"]) / args.steps
     ub = upsert_bytes(BATCH, DIM, CAP // 128, rows, False)
     find_roof = {"bound": "hbm", "achieved": fb / f_avg / 1e9, "peak": peak, "unit": "GB/s",
-                 "frac": fb / f_avg / 1e9 / peak, "traffic": None, "kernel": "find_kernel",
+                 "frac": fb / f_avg / 1e9 / peak, "traffic": ncu_traffic("find_kernel"),
+                 "kernel": "find_kernel",
                  "bytes_per_launch": fb, "avg_launch_s": f_avg, "peak_kind": peak_kind}
     up_roof = {"bound": "hbm", "achieved": ub / u_avg / 1e9, "peak": peak, "unit": "GB/s",
                "frac": ub / u_avg / 1e9 / peak, "traffic": None,
                "kernel": "insert_or_assign call (stage_kernel + upsert_single_kernel)",
                "bytes_per_launch": ub, "avg_launch_s": u_avg, "peak_kind": peak_kind}
     dominant = find_roof
+    try:
+        rates = probe_access_rates(DIM)
+        ff = find_access_floor(BATCH, DIM, hit_rate, CAP // 128, rates, peak)
+        uf = upsert_access_floor(BATCH, DIM, rows, CAP // 128, rates, peak)
+        access = {"random_reads_per_s": {f"{g}B": v for g, v in rates.items()},
+                  "find": {"floor_s": ff, "measured_s": f_avg, "frac": ff / f_avg},
+                  "insert_or_assign": {"floor_s": uf, "measured_s": u_avg, "frac": uf / u_avg},
+                  "note": "floor = random sector/row reads at the probed rates + streamed "
+                          "bytes at the copy peak"}
+    except Exception as exc:  # the probe is a measurement aid; the line stands without it
+        access = {"unavailable": str(exc)}
 
     # The other calls of the API on the same full table, one 2^20-key batch
     # each (median of 3, L2 flushed before each).
@@ -400,6 +477,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": dominant,
         "roofline_all": {"find": find_roof, "insert_or_assign": up_roof},
+        "access_ceiling": access,
         "per_step": {"insert_or_assign_s": statistics.mean(up_t), "find_s": statistics.mean(fi_t),
                      "find_bkvs": BATCH / f_avg / 1e9, "upsert_bkvs": BATCH / u_avg / 1e9,
                      "find_hit_rate": hit_rate, "op_counts": counts},

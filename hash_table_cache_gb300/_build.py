@@ -13,6 +13,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["table.cu", "find.cu", "upsert.cu", "export.cu", "no_alloc.cu"]
+# measurement helper used by bench.py, kept out of the table library
+PROBE_SOURCE = "access_probe.cu"
+PROBE_LIB = os.path.join(PKG, "libhkv_probe.so")
 
 
 def _nvcc():
@@ -47,18 +50,25 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
         return obj, r.stderr
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    with_probe = out == LIB
+    with ThreadPoolExecutor(max_workers=len(SOURCES) + 1) as ex:
+        results = list(ex.map(compile_one, SOURCES + ([PROBE_SOURCE] if with_probe else [])))
     if verbose:
         for _, err in results:
             print(err)
+    if with_probe:
+        _link([results[-1][0]], PROBE_LIB)
+        results = results[:-1]
+    _link([o for o, _ in results], out)
+    return out
+
+
+def _link(objs, out):
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *[o for o, _ in results]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    r = subprocess.run([_nvcc(), "-shared", *ARCH, "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, out)
-    return out
 
 
 if __name__ == "__main__":
