@@ -177,12 +177,6 @@ __device__ __forceinline__ ulonglong2 ld_nc_pair(const uint64_t* p) {
   return r;
 }
 
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned source) into
-// L2 by the copy engine of the SM; fire and forget, no register result.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
-
 // L2-coherent loads (bypass L1) for data other blocks may have written in
 // the same kernel.
 __device__ __forceinline__ uint64_t ld_cg_u64(const uint64_t* p) {

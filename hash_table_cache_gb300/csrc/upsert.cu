@@ -39,9 +39,6 @@ constexpr int kThreads = 256;
 #ifndef HKV_UPSERT_MIN_BLOCKS
 #define HKV_UPSERT_MIN_BLOCKS 3
 #endif
-#ifndef HKV_UPSERT_PREFETCH
-#define HKV_UPSERT_PREFETCH 1
-#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 constexpr int kSpinLimit = 1 << 20;
 
@@ -358,13 +355,6 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
        b += nwarps) {
     if (scr.mark && !scr.mark[b]) continue;  // no key of the batch here
     const uint64_t base = b * kSlots + lane * 4;
-    // The warp's next bucket: its key/score pairs and digest line go to L2
-    // now, so the loads at the top of the next iteration do not wait on DRAM.
-    if (HKV_UPSERT_PREFETCH && lane == 0 && b + nwarps < nb &&
-        (!scr.mark || scr.mark[b + nwarps])) {
-      prefetch_l2_bulk(key_at(t, (b + nwarps) * kSlots), kSlots * 16);
-      prefetch_l2_bulk(t.digests + (b + nwarps) * kSlots, kSlots);
-    }
     // This bucket's stage run: from lo, past a_end, up to the first free
     // position at or after a_end (linear probing leaves no gap in a run).
     const uint64_t lo = area_start(b, S, nb, scr.area_shift);
@@ -619,9 +609,6 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
           if (kLfu) st.einc[p] = scr.inc[(lo + 32ull * w + lane) & smask];
         }
         ne += __popc(m);
-        // the entry's input value row is read in phase C: start it now
-        if (HKV_UPSERT_PREFETCH && vec && we[w] != kNone)
-          prefetch_l2_bulk(values_in + static_cast<uint64_t>(we[w]) * t.dim, t.dim * 4);
       }
       __syncwarp();
       // (loops kept rolled: one copy of each phase keeps the code in cache)
@@ -1084,15 +1071,33 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
   return s;
 }
 
+namespace {
+
+// One launch clears every scratch array of a call: the map keys to EMPTY, the
+// map indices (and LFU sums) to 0, the counters and the bucket marks to 0.
+// map_size is a power of two >= 64, and every array starts 256-byte aligned.
+__global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s,
+                                                                 uint64_t mark_bytes) {
+  const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  const uint64_t pairs = s.map_size / 2;
+  for (uint64_t i = tid; i < pairs; i += stride) {
+    reinterpret_cast<ulonglong2*>(s.map_keys)[i] = make_ulonglong2(kEmptyKey, kEmptyKey);
+    reinterpret_cast<uint2*>(s.map_idx)[i] = make_uint2(0u, 0u);
+    if (s.inc) reinterpret_cast<ulonglong2*>(s.inc)[i] = make_ulonglong2(0ull, 0ull);
+  }
+  if (tid < 16) s.cursor[tid] = 0u;
+  if (s.mark)
+    for (uint64_t i = tid; i < mark_bytes; i += stride) s.mark[i] = 0;
+}
+
+}  // namespace
+
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(s.map_keys, 0xFF, static_cast<size_t>(s.map_size) * 8, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(s.map_idx, 0, static_cast<size_t>(s.map_size) * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(s.cursor, 0, 64, st);
-  if (e == cudaSuccess && kind == ScratchKind::kSingleUpsert && s.mark)
-    e = cudaMemsetAsync(s.mark, 0, num_buckets, st);
-  if (e == cudaSuccess && s.inc) e = cudaMemsetAsync(s.inc, 0, static_cast<size_t>(s.map_size) * 8, st);
-  return e;
+  const uint64_t mark_bytes = kind == ScratchKind::kSingleUpsert && s.mark ? num_buckets : 0;
+  clear_scratch_kernel<<<grid_for(s.map_size / 2), kThreads, 0, st>>>(s, mark_bytes);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
