@@ -16,6 +16,10 @@ SOURCES = ["table.cu", "find.cu", "upsert.cu", "export.cu", "no_alloc.cu"]
 # measurement helper used by bench.py, kept out of the table library
 PROBE_SOURCE = "access_probe.cu"
 PROBE_LIB = os.path.join(PKG, "libhkv_probe.so")
+# digest-ablation build of the library (find without the digest line, HKV
+# §5.4 Table 7): same ABI, used only by the ablation test and bench.py
+NODIGEST_LIB = os.path.join(PKG, "libhkv_nodigest.so")
+NODIGEST_FLAGS = ("-DHKV_FIND_NO_DIGEST=1",)
 
 
 def _nvcc():
@@ -29,12 +33,22 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
+def build_all(force: bool = False) -> None:
+    """libhkv.so (+ libhkv_probe.so) and the digest-ablation libhkv_nodigest.so,
+    compiled concurrently."""
+    with ThreadPoolExecutor(max_workers=2) as ex:
+        jobs = [ex.submit(build, force), ex.submit(build, force, False, NODIGEST_FLAGS, NODIGEST_LIB)]
+        for j in jobs:
+            j.result()
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB) -> str:
     """Compile every source and link `out` (default: the in-tree libhkv.so).
     `extra_flags` are passed to nvcc (e.g. -D tuning macros)."""
-    if not force and out == LIB and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
-        return LIB
-    build_dir = BUILD if out == LIB else out + ".objs"
+    if not force and out in (LIB, NODIGEST_LIB) and os.path.exists(out) and \
+            os.path.getmtime(out) >= _deps():
+        return out
+    build_dir = BUILD if out == LIB else os.path.join(BUILD, os.path.basename(out) + ".objs")
     os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",

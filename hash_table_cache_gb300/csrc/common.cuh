@@ -221,6 +221,18 @@ __device__ __forceinline__ uint32_t byte_match4(uint32_t w, uint32_t pat) {
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch (sm_90+).  A kernel launched with
+// launch_chained() may become resident while the previous kernel of its
+// stream is still running; pdl_wait() blocks until that kernel has completed
+// and its memory writes are visible, and is a no-op for a normal launch.
+// pdl_trigger() lets the next chained kernel be scheduled early.  Every
+// kernel here calls pdl_wait() before it touches global memory, so chaining
+// only hides the launch latency and the ramp between kernels.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Warp-aggregated atomic add of a per-lane contribution (any lane set).
 __device__ __forceinline__ void warp_add(unsigned long long* p, unsigned long long v) {
   unsigned long long s = v;

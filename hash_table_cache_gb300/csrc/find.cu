@@ -22,6 +22,9 @@ namespace {
 #ifndef HKV_FIND_MIN_BLOCKS
 #define HKV_FIND_MIN_BLOCKS 4
 #endif
+#ifndef HKV_FIND_NO_DIGEST
+#define HKV_FIND_NO_DIGEST 0
+#endif
 
 constexpr int kFindKeysPerTile = HKV_FIND_KEYS_PER_TILE;
 
@@ -90,6 +93,52 @@ __device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64
   }
 }
 
+// Digest ablation (HKV §5.4, Table 7): the same probe without the digest
+// line.  The tile compares the key against every slot's key: lane `sub`
+// reads the (key, score) pairs of slots sub, sub+8, ..., 16 bytes per lane
+// and 128 bytes per tile per step, until a step finds the key (a hit reads on
+// average half of the bucket's 2 KiB of pairs, a miss all of it).  Built only
+// with -DHKV_FIND_NO_DIGEST, for the ablation measurement.
+template <int U>
+__device__ __forceinline__ void tile_scan_many(const TableView& t, const uint64_t (&b)[U],
+                                               const uint64_t (&k)[U], const bool (&act)[U],
+                                               unsigned sub, unsigned tmask, int (&slot)[U],
+                                               uint64_t (&score)[U]) {
+  int hit[U];
+  uint64_t hs[U];
+  bool open[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    hit[u] = -1;
+    hs[u] = 0;
+    open[u] = act[u];
+  }
+  for (int c = 0; c < kSlots / 8; ++c) {
+    ulonglong2 p[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (open[u]) p[u] = ld_nc_pair(key_at(t, b[u] * kSlots + c * 8 + sub));
+    bool more = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (open[u] && p[u].x == k[u]) {
+        hit[u] = c * 8 + static_cast<int>(sub);
+        hs[u] = p[u].y;
+      }
+      open[u] = open[u] && !(__ballot_sync(tmask, hit[u] >= 0) & tmask);
+      more = more || open[u];
+    }
+    if (!more) break;
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
+    const int lead = bal ? __ffs(bal) - 1 : static_cast<int>(lane_id());
+    slot[u] = bal ? __shfl_sync(tmask, hit[u], lead) : -1;
+    score[u] = __shfl_sync(tmask, hs[u], lead);
+  }
+}
+
 // What a find writes per key besides the found flag (and the score).
 enum FindOut { kOutValues = 0, kOutNone = 1, kOutPointer = 2 };
 
@@ -100,6 +149,8 @@ template <bool kDual, int U, int kOut>
 __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
     find_kernel(TableView t, uint64_t n, const uint64_t* keys, float* values_out,
                 float** ptrs_out, uint8_t* found_out, uint64_t* scores_out, bool vec) {
+  pdl_wait();
+  pdl_trigger();
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
@@ -133,7 +184,11 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
     }
     int slot[U];
     uint64_t sc[U];
+#if HKV_FIND_NO_DIGEST
+    tile_scan_many<U>(t, b, k, act, sub, tmask, slot, sc);
+#else
     tile_probe_many<U>(t, b, k, pat, act, sub, tmask, slot, sc);
+#endif
     if (kDual) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -183,9 +238,8 @@ cudaError_t launch_find_u(const TableView& t, uint64_t n, const uint64_t* keys, 
   uint64_t blocks = (n * 8 + threads * U - 1) / (threads * U);
   const uint64_t cap = static_cast<uint64_t>(sm_count()) * per_sm;
   if (blocks > cap) blocks = cap;
-  find_kernel<kDual, U, kOut><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      t, n, keys, values_out, ptrs_out, found_out, scores_out, vec);
-  return cudaGetLastError();
+  return launch_chained(find_kernel<kDual, U, kOut>, static_cast<unsigned>(blocks), threads, st, t,
+                        n, keys, values_out, ptrs_out, found_out, scores_out, vec);
 }
 
 template <int kOut>

@@ -77,6 +77,25 @@ cudaError_t launch_clear_table(const TableView& t, cudaStream_t st);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Launch `kernel` on `st` with programmatic stream serialization, so it can be
+// scheduled while the stream's previous kernel drains (the kernel must call
+// pdl_wait() before touching memory that kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Runs insert_or_assign with caller-provided working memory (used by
 // hkv_insert_or_assign_noalloc); get_scratch(device, &ptr) yields it.
 struct NoAllocAccess {

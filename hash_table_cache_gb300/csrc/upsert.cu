@@ -136,11 +136,16 @@ __device__ __forceinline__ uint64_t stage_home(uint64_t h, uint64_t lo, uint64_t
   return lo + ((a & (a - 1)) == 0 ? (r & (a - 1)) : (r % a));
 }
 
-constexpr int kStageKeysPerThread = 1;
+#ifndef HKV_STAGE_KEYS_PER_THREAD
+#define HKV_STAGE_KEYS_PER_THREAD 1
+#endif
+constexpr int kStageKeysPerThread = HKV_STAGE_KEYS_PER_THREAD;
 
 __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScratch sc, uint64_t n,
                                                          const uint64_t* keys,
                                                          const uint64_t* inc_in) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int U = kStageKeysPerThread;
   const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
@@ -339,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     ScoreRule rule, bool vec, UpsertExtra ex) {
   (void)keys_in;  // entry keys come from the stage
   __shared__ BucketStage<kLfu> stage_all[kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const unsigned lane = lane_id();
   BucketStage<kLfu>& st = stage_all[threadIdx.x >> 5];
   auto score_of = [&](uint32_t e, uint64_t inc, bool resident, uint64_t old) -> uint64_t {
@@ -1030,7 +1037,12 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 namespace {
-uint64_t stage_entries(uint64_t n) { return next_pow2(n * 2 < 64 ? 64 : n * 2); }
+#ifndef HKV_STAGE_FACTOR
+#define HKV_STAGE_FACTOR 2
+#endif
+uint64_t stage_entries(uint64_t n) {
+  return next_pow2(n * HKV_STAGE_FACTOR < 64 ? 64 : n * HKV_STAGE_FACTOR);
+}
 }  // namespace
 
 size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind, bool lfu) {
@@ -1078,6 +1090,8 @@ namespace {
 // map_size is a power of two >= 64, and every array starts 256-byte aligned.
 __global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s,
                                                                  uint64_t mark_bytes) {
+  pdl_wait();
+  pdl_trigger();
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   const uint64_t pairs = s.map_size / 2;
@@ -1096,8 +1110,7 @@ __global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st) {
   const uint64_t mark_bytes = kind == ScratchKind::kSingleUpsert && s.mark ? num_buckets : 0;
-  clear_scratch_kernel<<<grid_for(s.map_size / 2), kThreads, 0, st>>>(s, mark_bytes);
-  return cudaGetLastError();
+  return launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, st, s, mark_bytes);
 }
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
@@ -1107,18 +1120,24 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
   const uint64_t* inc_in = rule.lfu() ? rule.in : nullptr;
   if (!t.dual) {
-    stage_kernel<<<grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread), kThreads, 0,
-                   st>>>(t, s, n, keys, inc_in);
+    cudaError_t e = launch_chained(stage_kernel,
+                                   grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread),
+                                   kThreads, st, t, s, n, keys, inc_in);
+    if (e != cudaSuccess) return e;
     const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
     if (rule.lfu()) {
-      upsert_single_kernel<true><<<grid, kThreads, 0, st>>>(t, s, keys, values, rule, vec, ex);
+      e = launch_chained(upsert_single_kernel<true>, grid, kThreads, st, t, s, keys, values, rule,
+                         vec, ex);
+      if (e != cudaSuccess) return e;
     } else {
       // one score per call unless the caller gives scores (kCustomized)
       ScoreRule r = rule;
       if (rule.policy != kCustomized) r.in = nullptr;
       if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
       r.policy = kCustomized;
-      upsert_single_kernel<false><<<grid, kThreads, 0, st>>>(t, s, keys, values, r, vec, ex);
+      e = launch_chained(upsert_single_kernel<false>, grid, kThreads, st, t, s, keys, values, r,
+                         vec, ex);
+      if (e != cudaSuccess) return e;
     }
   } else {
     dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, inc_in, t.stats);
