@@ -741,12 +741,16 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
-# Digest ablation (HKV §5.4, Table 7): find with and without the digest line
+# Build variants: the digest ablation (HKV §5.4, Table 7: find with and
+# without the digest line) and the pipelined bucket kernel (next bucket staged
+# in shared memory by bulk copies), each against the default build
 # ---------------------------------------------------------------------------
-def run_ablation_child(lib_path):
-    """find B-KV/s on the 2^22-slot, dim-32 table at load factors 0.5 and 1.0
-    for batches of 2^20 keys with 0%, 80% and 100% hits, using the library at
-    lib_path.  Prints one JSON object."""
+def run_ablation_child(lib_path, what):
+    """Times one build (the library at lib_path) on the 2^22-slot, dim-32
+    table with batches of 2^20 keys; prints one JSON object.  what="find":
+    find B-KV/s at load factors 0.5 and 1.0 with 0%, 80% and 100% hits.
+    what="upsert": insert_or_assign B-KV/s at load factor 1.0 on the headline
+    step mix (80% keys of the previous batch, 20% fresh), median of 10."""
     import torch
 
     import hash_table_cache_gb300 as hkv
@@ -757,48 +761,62 @@ def run_ablation_child(lib_path):
     keys = wl.unique_keys(3, 2 * CAP)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream()
+
+    def timed(fn):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        return a.elapsed_time(b) * 1e-3
+
     t = hkv.HashTable(CAP, DIM)
     pos, out = 0, {}
     vout = torch.empty((BATCH, DIM), dtype=torch.float32, device=dev)
     fo = torch.empty(BATCH, dtype=torch.uint8, device=dev)
     so = torch.empty(BATCH, dtype=torch.int64, device=dev)
-    for lam in (0.5, 1.0):
+    for lam in ((0.5, 1.0) if what == "find" else (1.0,)):
         while t.size() < lam * CAP and pos < keys.size:
             k = dk(keys[pos:pos + FILL_BATCH])
             t.insert_or_assign(k, wl.key_values_torch(k, DIM, salt=1), None)
             pos += FILL_BATCH
         res = t.export(with_values=False)[0].cpu().numpy().view(np.uint64)
-        for hit in (0.0, 0.8, 1.0):
-            q, _ = wl.hit_mix(4, res, 5, BATCH, hit, fresh_start=(1 + int(lam * 4)) << 24)
-            qd = dk(q)
-            for _ in range(3):
-                t.find(qd, vout, fo, so)
-            ts = []
-            for _ in range(5):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(st)
-                t.find(qd, vout, fo, so)
-                b.record(st)
-                b.synchronize()
-                ts.append(a.elapsed_time(b) * 1e-3)
-            out[f"lambda={lam} hits={hit}"] = BATCH / statistics.median(ts) / 1e9
+        if what == "find":
+            for hit in (0.0, 0.8, 1.0):
+                q, _ = wl.hit_mix(4, res, 5, BATCH, hit, fresh_start=(1 + int(lam * 4)) << 24)
+                qd = dk(q)
+                for _ in range(3):
+                    t.find(qd, vout, fo, so)
+                ts = [timed(lambda: t.find(qd, vout, fo, so)) for _ in range(5)]
+                out[f"find lambda={lam} hits={hit}"] = BATCH / statistics.median(ts) / 1e9
+        else:
+            batches, prev = [], res
+            for r in range(13):
+                q, _ = wl.hit_mix(100 + r, prev, 200, BATCH, HIT, fresh_start=r * BATCH)
+                prev = q
+                qd = dk(q)
+                batches.append((qd, wl.key_values_torch(qd, DIM, salt=3 + r)))
+            torch.cuda.synchronize()
+            ts = [timed(lambda: t.insert_or_assign(k, v, None)) for k, v in batches]
+            out["insert_or_assign lambda=1.0"] = BATCH / statistics.median(ts[3:]) / 1e9
     t.close()
     print(json.dumps(out))
 
 
 def run_ablation(args):
     from hash_table_cache_gb300 import _build
+    variant, what = {"digest": ("nodigest", "find"), "pipeline": ("pipeline", "upsert")}[args.ablation]
     res = {}
-    for name, lib in (("with_digest", _build.LIB), ("without_digest", _build.NODIGEST_LIB)):
-        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--ablation-child", lib],
-                           capture_output=True, text=True, check=True)
+    for name, lib in (("default_build", _build.LIB), (variant + "_build", _build.VARIANTS[variant][0])):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--ablation-child", lib,
+                            "--ablation-what", what], capture_output=True, text=True, check=True)
         res[name] = json.loads(r.stdout.strip().splitlines()[-1])
-    speedup = {k: res["with_digest"][k] / res["without_digest"][k] for k in res["with_digest"]}
-    print(json.dumps({"ablation": "digest", "unit": "B-KV/s (find)",
+    a, b = res["default_build"], res[variant + "_build"]
+    print(json.dumps({"ablation": args.ablation, "unit": "B-KV/s",
                       "config": {"workload": "single-bucket, capacity 2^22, dim 32 f32, batch 2^20",
-                                 "l2": "flushed before each timed find"},
-                      **res, "speedup_with_digest": speedup}))
+                                 "l2": "flushed before each timed call"},
+                      **res, "default_over_variant": {k: a[k] / b[k] for k in a}}))
 
 
 def main():
@@ -812,12 +830,14 @@ def main():
     ap.add_argument("--skip-sweep", action="store_true", help="only the headline steps")
     ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"],
                     help="workload; c2 (the default) is the headline line")
-    ap.add_argument("--ablation", choices=["digest"],
-                    help="measure find with and without the digest line instead")
+    ap.add_argument("--ablation", choices=["digest", "pipeline"],
+                    help="compare the default build with a variant build instead: find without "
+                         "the digest line, or the pipelined bucket kernel")
     ap.add_argument("--ablation-child", help=argparse.SUPPRESS)
+    ap.add_argument("--ablation-what", default="find", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.ablation_child:
-        run_ablation_child(args.ablation_child)
+        run_ablation_child(args.ablation_child, args.ablation_what)
     elif args.ablation:
         run_ablation(args)
     elif args.impl == "reference":

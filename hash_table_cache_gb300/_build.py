@@ -20,6 +20,11 @@ PROBE_LIB = os.path.join(PKG, "libhkv_probe.so")
 # §5.4 Table 7): same ABI, used only by the ablation test and bench.py
 NODIGEST_LIB = os.path.join(PKG, "libhkv_nodigest.so")
 NODIGEST_FLAGS = ("-DHKV_FIND_NO_DIGEST=1",)
+# pipelined build (the bucket kernel stages each warp's next bucket in shared
+# memory with bulk copies): same ABI, for the pipeline measurement only
+PIPELINE_LIB = os.path.join(PKG, "libhkv_pipeline.so")
+PIPELINE_FLAGS = ("-DHKV_UPSERT_PIPELINE=1",)
+VARIANTS = {"nodigest": (NODIGEST_LIB, NODIGEST_FLAGS), "pipeline": (PIPELINE_LIB, PIPELINE_FLAGS)}
 
 
 def _nvcc():
@@ -34,10 +39,11 @@ def _deps():
 
 
 def build_all(force: bool = False) -> None:
-    """libhkv.so (+ libhkv_probe.so) and the digest-ablation libhkv_nodigest.so,
-    compiled concurrently."""
-    with ThreadPoolExecutor(max_workers=2) as ex:
-        jobs = [ex.submit(build, force), ex.submit(build, force, False, NODIGEST_FLAGS, NODIGEST_LIB)]
+    """libhkv.so (+ libhkv_probe.so) and the measurement variants
+    (libhkv_nodigest.so, libhkv_pipeline.so), compiled concurrently."""
+    with ThreadPoolExecutor(max_workers=1 + len(VARIANTS)) as ex:
+        jobs = [ex.submit(build, force)]
+        jobs += [ex.submit(build, force, False, fl, lib) for lib, fl in VARIANTS.values()]
         for j in jobs:
             j.result()
 
@@ -45,7 +51,7 @@ def build_all(force: bool = False) -> None:
 def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB) -> str:
     """Compile every source and link `out` (default: the in-tree libhkv.so).
     `extra_flags` are passed to nvcc (e.g. -D tuning macros)."""
-    if not force and out in (LIB, NODIGEST_LIB) and os.path.exists(out) and \
+    if not force and out in (LIB, NODIGEST_LIB, PIPELINE_LIB) and os.path.exists(out) and \
             os.path.getmtime(out) >= _deps():
         return out
     build_dir = BUILD if out == LIB else os.path.join(BUILD, os.path.basename(out) + ".objs")

@@ -26,7 +26,7 @@ constexpr uint32_t kNone = 0xFFFFFFFFu;
 // Device-resident counters of one table.  Fields are updated with atomics.
 struct DeviceStats {
   unsigned long long reserved;   // reserved keys skipped
-  unsigned long long timeouts;   // keys abandoned after a bounded lock wait
+  unsigned long long timeouts;   // bounded waits that ran out (dual-mode locks, bucket copies)
   unsigned long long updated;
   unsigned long long admitted;
   unsigned long long evicted;
@@ -220,6 +220,51 @@ __device__ __forceinline__ uint32_t byte_match4(uint32_t w, uint32_t pat) {
 }
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+// ---------------------------------------------------------------------------
+// Bulk copies into shared memory by the copy engine (TMA, non-tensor form)
+// with completion on a shared-memory mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t arrivals) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(arrivals)
+               : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One arrival that also announces `bytes` of copies completing on `bar`.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load_smem(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later bulk copies into shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// One bounded probe of the barrier's phase `parity`; true once it completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 
 // Programmatic dependent launch (sm_90+).  A kernel launched with
 // launch_chained() may become resident while the previous kernel of its

@@ -238,8 +238,8 @@ cudaError_t launch_find_u(const TableView& t, uint64_t n, const uint64_t* keys, 
   uint64_t blocks = (n * 8 + threads * U - 1) / (threads * U);
   const uint64_t cap = static_cast<uint64_t>(sm_count()) * per_sm;
   if (blocks > cap) blocks = cap;
-  return launch_chained(find_kernel<kDual, U, kOut>, static_cast<unsigned>(blocks), threads, st, t,
-                        n, keys, values_out, ptrs_out, found_out, scores_out, vec);
+  return launch_chained(find_kernel<kDual, U, kOut>, static_cast<unsigned>(blocks), threads, 0, st,
+                        t, n, keys, values_out, ptrs_out, found_out, scores_out, vec);
 }
 
 template <int kOut>

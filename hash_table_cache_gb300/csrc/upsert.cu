@@ -39,6 +39,9 @@ constexpr int kThreads = 256;
 #ifndef HKV_UPSERT_MIN_BLOCKS
 #define HKV_UPSERT_MIN_BLOCKS 3
 #endif
+#ifndef HKV_UPSERT_PIPELINE
+#define HKV_UPSERT_PIPELINE 0
+#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 constexpr int kSpinLimit = 1 << 20;
 
@@ -236,6 +239,13 @@ struct alignas(16) BucketStage {
   uint8_t dnext[kSlots];            // next slot with the same digest (0xFF: end)
   uint8_t list[kSlots];             // free-slot list, later the dirty-slot list
   alignas(16) uint64_t einc[kLfu ? kWin * 32 : 2];  // summed increments (LFU policies)
+#if HKV_UPSERT_PIPELINE
+  // The warp's next bucket, brought in by the copy engine while this one is
+  // processed: its key/score pairs, its digest line and the copy's barrier.
+  alignas(128) ulonglong2 next_pairs[kSlots];
+  alignas(16) uint32_t next_dig[kSlots / 4];
+  alignas(8) uint64_t bar;
+#endif
 };
 #define HKV_STAGE_ALIGNED(L)                                                                     \
   static_assert(offsetof(BucketStage<L>, key) % 16 == 0 &&                                     \
@@ -246,6 +256,13 @@ struct alignas(16) BucketStage {
 HKV_STAGE_ALIGNED(false);
 HKV_STAGE_ALIGNED(true);
 #undef HKV_STAGE_ALIGNED
+#if HKV_UPSERT_PIPELINE
+static_assert(offsetof(BucketStage<false>, next_pairs) % 128 == 0 &&
+                  offsetof(BucketStage<true>, next_pairs) % 128 == 0 &&
+                  offsetof(BucketStage<false>, next_dig) % 16 == 0 &&
+                  offsetof(BucketStage<true>, next_dig) % 16 == 0,
+              "bulk-copy targets must be 16-byte aligned");
+#endif
 
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
@@ -338,12 +355,30 @@ __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, u
 // kLfu: the table sums increments (kLfu, kEpochLfu).  Otherwise every key of
 // the call gets rule.in[e] or the constant rule.clock (the host folds the
 // clock policies into that constant).
+//
+// Pipelined build (-DHKV_UPSERT_PIPELINE=1, the latency-hiding variant in
+// the spirit of HKV §4.3's Pipeline kernel): each warp keeps its next bucket
+// in flight.  While it works on bucket b, the copy engine moves the key/score
+// pairs (2 KiB) and the digest line of the next bucket it owns into shared
+// memory (cp.async.bulk, completion on an mbarrier).  The wait on the barrier
+// is bounded: if it runs out the warp counts a timeout, loads its buckets
+// directly from then on, and before exiting waits (bounded again) for the
+// copy still in flight.  Measured slower than the default build on GB300
+// (the kernel is bound by its instruction stream, not by the bucket loads),
+// so it is kept as a build option for that measurement only.
+constexpr int kCopyWaitLimit = 1 << 14;
+
 template <bool kLfu>
 __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
     ScoreRule rule, bool vec, UpsertExtra ex) {
   (void)keys_in;  // entry keys come from the stage
+#if HKV_UPSERT_PIPELINE
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  BucketStage<kLfu>* stage_all = reinterpret_cast<BucketStage<kLfu>*>(smem_raw);
+#else
   __shared__ BucketStage<kLfu> stage_all[kThreads / 32];
+#endif
   pdl_wait();
   pdl_trigger();
   const unsigned lane = lane_id();
@@ -358,9 +393,40 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
   const uint64_t S = scr.map_size, smask = S - 1;
   unsigned long long n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0;  // lane 0 only
 
+#if HKV_UPSERT_PIPELINE
+  // the warp's buckets with keys of the batch (sparse batches mark them)
+  auto owned_from = [&](uint64_t x) -> uint64_t {
+    while (x < nb && scr.mark && !scr.mark[x]) x += nwarps;
+    return x;
+  };
+  auto copy_bucket = [&](uint64_t x) {  // lane 0 only
+    mbar_arrive_expect_tx(&st.bar, kSlots * 16 + kSlots);
+    bulk_load_smem(st.next_pairs, key_at(t, x * kSlots), kSlots * 16, &st.bar);
+    bulk_load_smem(st.next_dig, t.digests + x * kSlots, kSlots, &st.bar);
+  };
+  auto wait_copy = [&](uint32_t par) {
+    bool done = false;
+    for (int it = 0; it < kCopyWaitLimit && !done; ++it) done = mbar_try_wait(&st.bar, par);
+    return __all_sync(0xFFFFFFFFu, done);
+  };
+  bool engine = true;      // the copy engine serves this warp
+  bool in_flight = false;  // a copy into next_* has not been waited for
+  uint32_t parity = 0;
+  uint64_t b = owned_from((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (lane == 0) mbar_init(&st.bar, 1);
+  __syncwarp();
+  if (b < nb) {
+    if (lane == 0) copy_bucket(b);
+    in_flight = true;
+  }
+  uint64_t b_next = 0;
+  for (; b < nb; b = b_next) {
+    b_next = owned_from(b + nwarps);
+#else
   for (uint64_t b = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nb;
        b += nwarps) {
     if (scr.mark && !scr.mark[b]) continue;  // no key of the batch here
+#endif
     const uint64_t base = b * kSlots + lane * 4;
     // This bucket's stage run: from lo, past a_end, up to the first free
     // position at or after a_end (linear probing leaves no gap in a run).
@@ -368,11 +434,32 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
 
     // Loads: the bucket (the lane's four key/score pairs and digest bytes)
-    // and the first kWin chunks of the run, all issued before any use.
+    // and the first kWin chunks of the run, all issued before any use.  The
+    // pipelined build takes the bucket from the copy engine's buffer.
     ulonglong2 kv[4];
+    uint32_t dw;
+#if HKV_UPSERT_PIPELINE
+    bool have = false;
+    if (engine) {
+      if (wait_copy(parity)) {
+        parity ^= 1u;
+        in_flight = false;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) kv[q] = *reinterpret_cast<const ulonglong2*>(key_at(t, base + q));
-    const uint32_t dw = *reinterpret_cast<const uint32_t*>(t.digests + base);
+        for (int q = 0; q < 4; ++q) kv[q] = st.next_pairs[lane * 4 + q];
+        dw = st.next_dig[lane];
+        have = true;
+      } else {
+        engine = false;
+        if (lane == 0) atomicAdd(&t.stats->timeouts, 1ull);
+      }
+    }
+    if (!have)
+#endif
+    {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) kv[q] = *reinterpret_cast<const ulonglong2*>(key_at(t, base + q));
+      dw = *reinterpret_cast<const uint32_t*>(t.digests + base);
+    }
     const uint64_t nw_need = (a_end - lo) / 32 + 1;
     const uint32_t nw = nw_need < kWin ? static_cast<uint32_t>(nw_need) : kWin;
     uint64_t wk[kWin];
@@ -387,6 +474,16 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         wr[w] = scr.map_idx[j];
       }
     }
+#if HKV_UPSERT_PIPELINE
+    __syncwarp();  // every lane has read the buffer: refill it
+    if (engine && b_next < nb) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        copy_bucket(b_next);
+      }
+      in_flight = true;
+    }
+#endif
     *reinterpret_cast<ulonglong2*>(&st.key[lane * 4]) = make_ulonglong2(kv[0].x, kv[1].x);
     *reinterpret_cast<ulonglong2*>(&st.key[lane * 4 + 2]) = make_ulonglong2(kv[2].x, kv[3].x);
     *reinterpret_cast<ulonglong2*>(&st.score[lane * 4]) = make_ulonglong2(kv[0].y, kv[1].y);
@@ -703,6 +800,9 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     }
     __syncwarp();
   }
+#if HKV_UPSERT_PIPELINE
+  if (in_flight) wait_copy(parity);  // only after a timed-out wait: let the copy land first
+#endif
   if (lane == 0) {
     if (n_upd) atomicAdd(&t.stats->updated, n_upd);
     if (n_adm) atomicAdd(&t.stats->admitted, n_adm);
@@ -1110,7 +1210,7 @@ __global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st) {
   const uint64_t mark_bytes = kind == ScratchKind::kSingleUpsert && s.mark ? num_buckets : 0;
-  return launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, st, s, mark_bytes);
+  return launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, 0, st, s, mark_bytes);
 }
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
@@ -1122,12 +1222,17 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   if (!t.dual) {
     cudaError_t e = launch_chained(stage_kernel,
                                    grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread),
-                                   kThreads, st, t, s, n, keys, inc_in);
+                                   kThreads, 0, st, t, s, n, keys, inc_in);
     if (e != cudaSuccess) return e;
     const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
     if (rule.lfu()) {
-      e = launch_chained(upsert_single_kernel<true>, grid, kThreads, st, t, s, keys, values, rule,
-                         vec, ex);
+      const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kThreads / 32) : 0;
+      if (smem) e = cudaFuncSetAttribute(upsert_single_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      e = launch_chained(upsert_single_kernel<true>, grid, kThreads, smem, st, t, s, keys, values,
+                         rule, vec, ex);
       if (e != cudaSuccess) return e;
     } else {
       // one score per call unless the caller gives scores (kCustomized)
@@ -1135,8 +1240,13 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
       if (rule.policy != kCustomized) r.in = nullptr;
       if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
       r.policy = kCustomized;
-      e = launch_chained(upsert_single_kernel<false>, grid, kThreads, st, t, s, keys, values, r,
-                         vec, ex);
+      const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kThreads / 32) : 0;
+      if (smem) e = cudaFuncSetAttribute(upsert_single_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      e = launch_chained(upsert_single_kernel<false>, grid, kThreads, smem, st, t, s, keys, values,
+                         r, vec, ex);
       if (e != cudaSuccess) return e;
     }
   } else {
