@@ -536,6 +536,11 @@ def run_other(args):
 
     nsteps = args.warmup + args.steps
     times, nkeys, launches = [], [], 0
+
+    def mark_timed(s):
+        """NVTX range "timed" over the timed steps (for a profiler)."""
+        if s == args.warmup:
+            torch.cuda.nvtx.range_push("timed")
     if cfg == "c1":
         cap, dim, n = 65536, 8, 65536
         keys = wl.unique_keys(1, n)
@@ -547,6 +552,7 @@ def run_other(args):
         kd, qd = dk(keys), dk(q)
         t = None
         for s in range(nsteps):
+            mark_timed(s)
             if t is not None:
                 t.close()
             t = hkv.HashTable(cap, dim)
@@ -567,6 +573,7 @@ def run_other(args):
         prefill(t, dim, 6)
         z = wl.Zipf(1.05, 1 << 32)
         for s in range(nsteps):
+            mark_timed(s)
             u = dk(wl.zipf_keys(7 + s, n, 1.05, 1 << 32))
             f = dk(wl.zipf_keys(10007 + s, n, 1.05, 1 << 32))
             uv = wl.key_values_torch(u, dim, salt=100 + s)
@@ -589,6 +596,7 @@ def run_other(args):
         base = inserted.size
         more = wl.unique_keys(9, nsteps * n)
         for s in range(nsteps):
+            mark_timed(s)
             u = dk(more[s * n:(s + 1) * n])
             usc = dk(wl.stream(90, n, s * n) >> np.uint64(2))
             f = dk(wl.choice(10 + s, inserted, n))
@@ -619,6 +627,7 @@ def run_other(args):
                 for _ in range(3)]
         torch.cuda.synchronize()
         for s in range(nsteps):
+            mark_timed(s)
             a, b = ev(), ev()
             flush.zero_()
             a.record(stream)
@@ -639,6 +648,7 @@ def run_other(args):
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(5 * n)
         launches = 3 + 2 + 2
+    torch.cuda.nvtx.range_pop()
     counts = t.op_counts()
     total = sum(times)
     line = {

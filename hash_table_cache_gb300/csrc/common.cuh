@@ -36,6 +36,16 @@ struct DeviceStats {
   unsigned long long fills;      // dual mode: entries placed in free slots by the current call
 };
 
+// Dual mode: per bucket, its occupancy and the lowest score in it, as of the
+// last upsert pass that processed the bucket (erase keeps the count exact;
+// assign may leave min_score below the true minimum).  Upserts use them only
+// to choose between a key's two buckets, never to decide admission.
+struct BucketSummary {
+  unsigned long long min_score;
+  unsigned int count;
+  unsigned int pad;
+};
+
 // Everything a kernel needs to address the table; passed by value.
 struct TableView {
   uint8_t* digests;
@@ -47,7 +57,7 @@ struct TableView {
   uint64_t bucket_mask;   // num_buckets - 1 when a power of two, else 0
   uint32_t dim;
   uint32_t dual;
-  uint32_t* locks;        // dual mode: one word per bucket
+  BucketSummary* summary; // dual mode: one per bucket (routing hints)
   DeviceStats* stats;
 };
 
@@ -356,6 +366,54 @@ __device__ __forceinline__ int tile_probe(const TableView& t, uint64_t b, uint64
   const unsigned bal = __ballot_sync(tmask, hit >= 0) & tmask;
   if (!bal) return -1;
   return __shfl_sync(tmask, hit, __ffs(bal) - 1);
+}
+
+// Probe both candidate buckets of a dual-mode key at once (HKV §3.4: two
+// fixed-length line loads): the two digest lines are loaded together, then
+// the candidates of b1 and of b2 are confirmed.  Returns the slot and sets
+// `b` to the bucket holding the key, or returns -1.
+template <bool kNC>
+__device__ __forceinline__ int tile_probe_pair(const TableView& t, uint64_t b1, uint64_t b2,
+                                               uint64_t key, uint32_t pat, unsigned sub,
+                                               unsigned tmask, uint64_t& b) {
+  const uint8_t* d1 = t.digests + b1 * kSlots + sub * 16;
+  const uint8_t* d2 = t.digests + b2 * kSlots + sub * 16;
+  uint4 g1, g2;
+  if (kNC) {
+    g1 = ld_nc_v4(d1);
+    g2 = ld_nc_v4(d2);
+  } else {
+    g1 = ld_cg_v4(d1);
+    g2 = ld_cg_v4(d2);
+  }
+  uint32_t m1 = byte_match4(g1.x, pat) | (byte_match4(g1.y, pat) << 4) |
+                (byte_match4(g1.z, pat) << 8) | (byte_match4(g1.w, pat) << 12);
+  uint32_t m2 = byte_match4(g2.x, pat) | (byte_match4(g2.y, pat) << 4) |
+                (byte_match4(g2.z, pat) << 8) | (byte_match4(g2.w, pat) << 12);
+  int hit = -1;
+  uint32_t which = 0;
+  const uint64_t* k1 = t.slots + 2 * (b1 * kSlots + sub * 16);
+  const uint64_t* k2 = t.slots + 2 * (b2 * kSlots + sub * 16);
+  while (m1 | m2) {
+    const bool first = m1 != 0;
+    uint32_t& m = first ? m1 : m2;
+    const int bit = __ffs(m) - 1;
+    m &= m - 1;
+    const uint64_t* kp = (first ? k1 : k2) + 2 * bit;
+    const uint64_t kk = kNC ? ld_nc_u64(kp) : ld_cg_u64(kp);
+    if (kk == key) {
+      hit = static_cast<int>(sub * 16 + bit);
+      which = first ? 1u : 2u;
+      break;
+    }
+  }
+  // a key sits in at most one of its buckets
+  const unsigned bal = __ballot_sync(tmask, hit >= 0) & tmask;
+  if (!bal) return -1;
+  const int lead = __ffs(bal) - 1;
+  which = __shfl_sync(tmask, which, lead);
+  b = which == 1u ? b1 : b2;
+  return __shfl_sync(tmask, hit, lead);
 }
 
 }  // namespace hkv

@@ -58,7 +58,8 @@ cudaError_t launch_clear_table(const TableView& t, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(t.slots, 0xFF, slots * 16, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(t.digests, 0, slots, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(t.stats, 0, sizeof(DeviceStats), st);
-  if (e == cudaSuccess && t.locks) e = cudaMemsetAsync(t.locks, 0, t.num_buckets * 4, st);
+  if (e == cudaSuccess && t.summary)
+    e = cudaMemsetAsync(t.summary, 0, t.num_buckets * sizeof(BucketSummary), st);
   return e;
 }
 

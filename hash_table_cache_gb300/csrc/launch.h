@@ -20,9 +20,20 @@ struct UpsertScratch {
   uint32_t* cursor;     // small counters (0-initialised)
   uint8_t* mark;        // single mode, sparse batches: one byte per table bucket,
                         // 1 = holds batch keys (null for dense batches)
-  uint32_t* group;      // dual mode: indices of the batch's absent keys
+  uint8_t* absent;      // dual mode: per dedup-map entry, 1 = the key was absent
+                        // before the call (written for every entry in use)
+  uint32_t* retry;      // dual mode: absent keys displaced in the first pass
   uint64_t* inc;        // LFU policies: summed increments per map entry,
                         // 0-initialised (null under the other policies)
+  // The stage read by the bucket kernel: one run of positions per bucket.
+  // Single mode stages straight into the dedup arrays (stage_keys = map_keys,
+  // stage_idx = map_idx, stage_inc = inc, stage_bkt = null); dual mode routes
+  // each absent key to one of its two buckets and stages it in a second set
+  // of arrays, with the chosen bucket in stage_bkt.
+  uint64_t* stage_keys;
+  uint32_t* stage_idx;
+  uint32_t* stage_bkt;
+  uint64_t* stage_inc;
 };
 
 // What a call needs scratch for.
@@ -51,6 +62,7 @@ cudaError_t launch_find_ptr(const TableView& t, uint64_t n, const uint64_t* keys
 // untouched; insert_and_evict reports the pre-call residents it displaces.
 struct UpsertExtra {
   bool update_resident = true;
+  bool collect_retry = false;  // dual mode, first bucket pass: list displaced keys
   uint64_t* ev_keys = nullptr;
   float* ev_values = nullptr;
   uint64_t* ev_scores = nullptr;

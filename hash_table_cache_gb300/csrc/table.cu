@@ -154,7 +154,7 @@ void release(hkv_table* t) {
   cudaFree(t->v.digests);
   cudaFree(t->v.slots);
   cudaFree(t->v.values_hbm);
-  cudaFree(t->v.locks);
+  cudaFree(t->v.summary);
   cudaFree(t->v.stats);
   if (t->host_slab) cudaFreeHost(t->host_slab);
   delete t;
@@ -276,7 +276,7 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
   if (e == cudaSuccess) e = cudaMalloc(&v.slots, capacity * 16);
   if (e == cudaSuccess) e = cudaMalloc(&v.stats, sizeof(hkv::DeviceStats));
   if (e == cudaSuccess && hbm_rows) e = cudaMalloc(&v.values_hbm, hbm_rows * 4ull * dim);
-  if (e == cudaSuccess && dual) e = cudaMalloc(&v.locks, nb * 4);
+  if (e == cudaSuccess && dual) e = cudaMalloc(&v.summary, nb * sizeof(hkv::BucketSummary));
   if (e == cudaSuccess && hbm_rows < capacity) {
     e = cudaHostAlloc(reinterpret_cast<void**>(&t->host_slab), (capacity - hbm_rows) * 4ull * dim,
                       cudaHostAllocMapped | cudaHostAllocPortable);

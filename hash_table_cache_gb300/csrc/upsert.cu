@@ -23,11 +23,12 @@
 // of a bucket depends only on its residents and its keys in the batch, never
 // on thread scheduling, so it equals the oracle's serial result exactly.
 //
-// Dual mode couples two buckets per key, so ownership cannot be partitioned:
-// the batch is de-duplicated in a scratch map, resident keys are updated in
-// place by a tile kernel, then each absent key is placed by one warp holding
-// locks on both candidate buckets (taken in increasing bucket order, bounded
-// spin).
+// Dual mode couples two buckets per key.  The batch is de-duplicated in a
+// scratch map; a tile kernel updates resident keys in place and routes each
+// absent key to one of its buckets by Algorithm 3's rules on per-bucket
+// summaries; the same bucket kernel then places every bucket's routed keys;
+// keys that pass displaces are routed once more and placed in a second pass.
+// No locks: every bucket still has one owner per pass.
 #include <cstddef>
 
 #include "launch.h"
@@ -43,7 +44,6 @@ constexpr int kThreads = 256;
 #define HKV_UPSERT_PIPELINE 0
 #endif
 constexpr uint32_t kHitMark = 0x80000000u;
-constexpr int kSpinLimit = 1 << 20;
 
 __device__ __forceinline__ uint32_t map_home(uint64_t key, uint32_t mask) {
   return static_cast<uint32_t>(hash64(key) >> 32) & mask;
@@ -198,16 +198,12 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
   warp_add(&t.stats->reserved, reserved);
 }
 
-// Rank order of dual mode (HKV Algorithm 3 arg-min and its strict admission,
-// ties by key): true when (s1,k1) < (s2,k2).
-__device__ __forceinline__ bool rank_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
-  return s1 < s2 || (s1 == s2 && k1 < k2);
-}
-
 // Rank order of single mode: (score, new, key), where `new` marks an entry
 // placed in the bucket by the current call.  HKV Algorithm 2 admits an absent
 // key when its score is >= the bucket minimum, so an incoming key outranks an
 // older entry of equal score; the key orders entries of equal score and age.
+// Dual mode ranks by (score, key) (Algorithm 3 admits on score > minimum, the
+// key breaks ties): the same order with every `new` bit 0.
 __device__ __forceinline__ bool rank3_less(uint64_t s1, uint32_t n1, uint64_t k1, uint64_t s2,
                                            uint32_t n2, uint64_t k2) {
   if (s1 != s2) return s1 < s2;
@@ -309,10 +305,10 @@ template <class Stage>
 __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, uint32_t E,
                                                uint32_t f0, uint32_t f1, uint32_t f2, uint32_t f3,
                                                uint32_t mf, bool pending, uint64_t se,
-                                               uint64_t ke) {
+                                               uint64_t ke, bool with_new) {
   constexpr uint32_t kGone = 0xFFFFFFFFu;
   uint32_t rf[4] = {f0, f1, f2, f3};
-  const uint32_t fw = st->fresh[lane >> 3] >> ((lane * 4) & 31);
+  const uint32_t fw = with_new ? st->fresh[lane >> 3] >> ((lane * 4) & 31) : 0u;
   uint32_t rem = 0;
   for (uint32_t x = 0; x < E; ++x) {
     const uint32_t lf = min(min(min(rf[0], rf[1]), min(rf[2], rf[3])), mf);
@@ -326,7 +322,7 @@ __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, u
       if (!((eq >> q) & 1u)) continue;
       const uint64_t cs = q < 4 ? st->score[lane * 4 + q] : se;
       const uint64_t ck = q < 4 ? st->key[lane * 4 + q] : ke;
-      const uint32_t cn = q < 4 ? (fw >> q) & 1u : 1u;
+      const uint32_t cn = q < 4 ? (fw >> q) & 1u : (with_new ? 1u : 0u);
       if (!bbit || rank3_less(cs, cn, ck, bs, bn, bk)) {
         bs = cs;
         bk = ck;
@@ -355,6 +351,11 @@ __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, u
 // kLfu: the table sums increments (kLfu, kEpochLfu).  Otherwise every key of
 // the call gets rule.in[e] or the constant rule.clock (the host folds the
 // clock policies into that constant).
+// kDual: the buckets of a dual-mode table, whose stage holds the absent keys
+// routed to each bucket (their chosen bucket in stage_bkt).  Ranks are then
+// (score, key) (Algorithm 3), no key is resident (phase A is skipped), the
+// batch counts come from a later kernel (this one only adds the free slots it
+// fills), and the kernel leaves each bucket's summary.
 //
 // Pipelined build (-DHKV_UPSERT_PIPELINE=1, the latency-hiding variant in
 // the spirit of HKV §4.3's Pipeline kernel): each warp keeps its next bucket
@@ -366,9 +367,11 @@ __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, u
 // copy still in flight.  Measured slower than the default build on GB300
 // (the kernel is bound by its instruction stream, not by the bucket loads),
 // so it is kept as a build option for that measurement only.
+#if HKV_UPSERT_PIPELINE
 constexpr int kCopyWaitLimit = 1 << 14;
+#endif
 
-template <bool kLfu>
+template <bool kLfu, bool kDual>
 __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
     ScoreRule rule, bool vec, UpsertExtra ex) {
@@ -391,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
   const uint64_t nb = t.num_buckets;
   const unsigned sub = lane & 7u;
   const uint64_t S = scr.map_size, smask = S - 1;
-  unsigned long long n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0;  // lane 0 only
+  unsigned long long n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0, n_fill = 0;  // lane 0 only
+  constexpr uint32_t kNewBit = kDual ? 0u : 1u;  // rank (score, new, key) or (score, key)
 
 #if HKV_UPSERT_PIPELINE
   // the warp's buckets with keys of the batch (sparse batches mark them)
@@ -463,15 +467,17 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     const uint64_t nw_need = (a_end - lo) / 32 + 1;
     const uint32_t nw = nw_need < kWin ? static_cast<uint32_t>(nw_need) : kWin;
     uint64_t wk[kWin];
-    uint32_t wr[kWin];
+    uint32_t wr[kWin], wb[kWin];
 #pragma unroll
     for (int w = 0; w < kWin; ++w) {
       wk[w] = kEmptyKey;
       wr[w] = 0;
+      wb[w] = 0;
       if (w < static_cast<int>(nw)) {
         const uint64_t j = (lo + 32ull * w + lane) & smask;
-        wk[w] = scr.map_keys[j];
-        wr[w] = scr.map_idx[j];
+        wk[w] = scr.stage_keys[j];
+        wr[w] = scr.stage_idx[j];
+        if (kDual) wb[w] = scr.stage_bkt[j];
       }
     }
 #if HKV_UPSERT_PIPELINE
@@ -490,14 +496,18 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     *reinterpret_cast<ulonglong2*>(&st.score[lane * 4 + 2]) = make_ulonglong2(kv[2].y, kv[3].y);
     *reinterpret_cast<uint4*>(&st.occ[lane * 4]) = make_uint4(kNone, kNone, kNone, kNone);
     st.dig[lane] = dw;
-    // Reverse digest index of the bucket: a chain of slots per digest value.
-    reinterpret_cast<uint4*>(st.dhead)[2 * lane] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
-    reinterpret_cast<uint4*>(st.dhead)[2 * lane + 1] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
-    __syncwarp();
+    // Reverse digest index of the bucket: a chain of slots per digest value
+    // (phase A's lookup; dual mode routes only absent keys and skips it).
+    if (!kDual) {
+      reinterpret_cast<uint4*>(st.dhead)[2 * lane] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
+      reinterpret_cast<uint4*>(st.dhead)[2 * lane + 1] = make_uint4(0xFF, 0xFF, 0xFF, 0xFF);
+      __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t d = (dw >> (8 * q)) & 0xFFu;
-      if (d) st.dnext[lane * 4 + q] = static_cast<uint8_t>(atomicExch(&st.dhead[d], lane * 4 + q));
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t d = (dw >> (8 * q)) & 0xFFu;
+        if (d)
+          st.dnext[lane * 4 + q] = static_cast<uint8_t>(atomicExch(&st.dhead[d], lane * 4 + q));
+      }
     }
     if (lane < 4) st.fresh[lane] = 0;
 
@@ -505,19 +515,21 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     // a key of bucket b before the end of the run (else kNone).  `stop`
     // carries the run end across chunks.
     bool run_ended = false;
-    auto entry_of = [&](uint64_t c, uint64_t key, uint32_t raw) -> uint32_t {
+    auto entry_of = [&](uint64_t c, uint64_t key, uint32_t raw, uint32_t bkt) -> uint32_t {
       const uint64_t j = lo + 32ull * c + lane;
       const bool empty = key == kEmptyKey;
       const unsigned stopm = __ballot_sync(0xFFFFFFFFu, empty && j >= a_end);
       const bool before = !run_ended && (stopm == 0 || lane < static_cast<unsigned>(__ffs(stopm) - 1));
       if (stopm) run_ended = true;
       if (32ull * (c + 1) >= S) run_ended = true;
-      const bool mine = !empty && before && bucket_of_hash(t, hash64(key)) == b;
+      const bool mine = !empty && before &&
+                        (kDual ? bkt == static_cast<uint32_t>(b) : bucket_of_hash(t, hash64(key)) == b);
       return mine ? (raw & ~kHitMark) - 1 : kNone;
     };
     uint32_t we[kWin];
 #pragma unroll
-    for (int w = 0; w < kWin; ++w) we[w] = w < static_cast<int>(nw) ? entry_of(w, wk[w], wr[w]) : kNone;
+    for (int w = 0; w < kWin; ++w)
+      we[w] = w < static_cast<int>(nw) ? entry_of(w, wk[w], wr[w], wb[w]) : kNone;
     const bool in_window = run_ended;  // the run ends inside the loaded chunks
     __syncwarp();
 
@@ -572,7 +584,10 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       }
       const uint32_t placed = min(static_cast<uint32_t>(__popc(mm)), nfree - used);
       used += placed;
-      if (lane == 0) n_adm += placed;
+      if (lane == 0) {
+        n_adm += placed;
+        n_fill += placed;
+      }
       bool pending = miss && rank >= nfree;  // this lane's absent key still competes
       const unsigned em = __ballot_sync(0xFFFFFFFFu, pending);
       if (!em) return;
@@ -609,8 +624,9 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       };
       uint32_t rf[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) rf[q] = fkey(s4[q], (fw >> q) & 1u, st.key[lane * 4 + q]);
-      const uint32_t mf0 = pending ? fkey(se, 1u, ke) : kGone;
+      for (int q = 0; q < 4; ++q)
+        rf[q] = fkey(s4[q], (fw >> q) & kNewBit, st.key[lane * 4 + q]);
+      const uint32_t mf0 = pending ? fkey(se, kNewBit, ke) : kGone;
       const bool pending0 = pending;
       uint32_t mf = mf0;
       // E extractions of the union's minimum.  Fast pass: every element equal
@@ -631,10 +647,11 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       if (__reduce_add_sync(0xFFFFFFFFu, out) != E) {
         // Equal 31-bit keys met at the front: redo with exact ranks.
         const ExactOut r = extract_exact(
-            &st, lane, E, fkey(s4[0], fw & 1u, st.key[lane * 4]),
-            fkey(s4[1], (fw >> 1) & 1u, st.key[lane * 4 + 1]),
-            fkey(s4[2], (fw >> 2) & 1u, st.key[lane * 4 + 2]),
-            fkey(s4[3], (fw >> 3) & 1u, st.key[lane * 4 + 3]), mf0, pending0, se, ke);
+            &st, lane, E, fkey(s4[0], fw & kNewBit, st.key[lane * 4]),
+            fkey(s4[1], (fw >> 1) & kNewBit, st.key[lane * 4 + 1]),
+            fkey(s4[2], (fw >> 2) & kNewBit, st.key[lane * 4 + 2]),
+            fkey(s4[3], (fw >> 3) & kNewBit, st.key[lane * 4 + 3]), mf0, pending0, se, ke,
+            kNewBit != 0);
         rem = r.rem;
         pending = r.pending;
       }
@@ -665,6 +682,24 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
             }
           }
         }
+      }
+      if (kDual && ex.collect_retry) {
+        // keys of the batch this pass displaced (rejected absent keys and
+        // entries it placed and then lost) are routed once more
+        uint32_t mine = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mine += (rem >> q) & (fw >> q) & 1u;
+        const bool rej = pending0 && !pending;
+        mine += rej ? 1u : 0u;
+        uint32_t tot;
+        uint32_t at = prefix_small(mine, tot);
+        uint32_t base_r = 0;
+        if (lane == 0 && tot) base_r = atomicAdd(scr.cursor + 4, tot);
+        base_r = __shfl_sync(0xFFFFFFFFu, base_r, 0) + at;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if ((rem >> q) & (fw >> q) & 1u) scr.retry[base_r++] = st.occ[lane * 4 + q];
+        if (rej) scr.retry[base_r] = e;
       }
       const uint32_t n_ev = __reduce_add_sync(0xFFFFFFFFu, ev);
       const uint32_t n_fr = __reduce_add_sync(0xFFFFFFFFu, fr);
@@ -710,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
           const uint32_t p = ne + __popc(m & lanemask_lt());
           st.ekey[p] = wk[w];
           st.eidx[p] = we[w];
-          if (kLfu) st.einc[p] = scr.inc[(lo + 32ull * w + lane) & smask];
+          if (kLfu) st.einc[p] = scr.stage_inc[(lo + 32ull * w + lane) & smask];
         }
         ne += __popc(m);
       }
@@ -718,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       // (loops kept rolled: one copy of each phase keeps the code in cache)
       uint32_t hits = 0;  // bit c: this lane's entry of dense chunk c hit
 #pragma unroll 1
-      for (uint32_t c = 0; 32u * c < ne; ++c) {
+      for (uint32_t c = 0; !kDual && 32u * c < ne; ++c) {
         const bool v = 32u * c + lane < ne;
         const uint64_t inc = kLfu && v ? st.einc[32 * c + lane] : 0ull;
         if (phase_a(v ? st.eidx[32 * c + lane] : kNone, v ? st.ekey[32 * c + lane] : kEmptyKey,
@@ -740,11 +775,11 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       run_ended = false;
       for (uint64_t c = 0; !run_ended; ++c) {
         const uint64_t j = (lo + 32ull * c + lane) & smask;
-        const uint64_t key = scr.map_keys[j];
-        const uint32_t raw = scr.map_idx[j];
-        const uint32_t e = entry_of(c, key, raw);
-        if (phase_a(e, key, kLfu && e != kNone ? entry_inc(scr, static_cast<uint32_t>(j)) : 0ull))
-          scr.map_idx[j] = raw | kHitMark;
+        const uint64_t key = scr.stage_keys[j];
+        const uint32_t raw = scr.stage_idx[j];
+        const uint32_t e = entry_of(c, key, raw, kDual ? scr.stage_bkt[j] : 0u);
+        if (!kDual && phase_a(e, key, kLfu && e != kNone ? scr.stage_inc[j] : 0ull))
+          scr.stage_idx[j] = raw | kHitMark;
         nch = c + 1;
       }
       __syncwarp();
@@ -752,14 +787,32 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       run_ended = false;
       for (uint64_t c = 0; c < nch; ++c) {
         const uint64_t j = (lo + 32ull * c + lane) & smask;
-        const uint64_t key = scr.map_keys[j];
-        const uint32_t raw = scr.map_idx[j];
-        const uint32_t e = entry_of(c, key, raw);
+        const uint64_t key = scr.stage_keys[j];
+        const uint32_t raw = scr.stage_idx[j];
+        const uint32_t e = entry_of(c, key, raw, kDual ? scr.stage_bkt[j] : 0u);
         phase_b(e, key, e != kNone && !(raw & kHitMark),
-                kLfu && e != kNone ? entry_inc(scr, static_cast<uint32_t>(j)) : 0ull);
+                kLfu && e != kNone ? scr.stage_inc[j] : 0ull);
       }
     }
     __syncwarp();
+
+    if (kDual) {  // the bucket's summary for the next routing
+      uint32_t cnt = 0;
+      uint64_t mn = ~0ull;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (st.key[lane * 4 + q] == kEmptyKey) continue;
+        ++cnt;
+        mn = min(mn, st.score[lane * 4 + q]);
+      }
+      unsigned sel;
+      mn = warp_min_u64(mn, true, sel);
+      cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+      if (lane == 0) {
+        t.summary[b].min_score = cnt ? mn : 0ull;
+        t.summary[b].count = cnt;
+      }
+    }
 
     // Phase C: write back the lane's changed slots and digest bytes, then
     // copy the value rows of the final occupants.
@@ -804,22 +857,85 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
   if (in_flight) wait_copy(parity);  // only after a timed-out wait: let the copy land first
 #endif
   if (lane == 0) {
-    if (n_upd) atomicAdd(&t.stats->updated, n_upd);
-    if (n_adm) atomicAdd(&t.stats->admitted, n_adm);
-    if (n_evi) atomicAdd(&t.stats->evicted, n_evi);
-    if (n_rej) atomicAdd(&t.stats->rejected, n_rej);
-    if (n_adm != n_evi) atomicAdd(&t.stats->size, n_adm - n_evi);
+    if (kDual) {  // dual_count_kernel / dual_finish_kernel produce the counts
+      if (n_fill) atomicAdd(&t.stats->fills, n_fill);
+    } else {
+      if (n_upd) atomicAdd(&t.stats->updated, n_upd);
+      if (n_adm) atomicAdd(&t.stats->admitted, n_adm);
+      if (n_evi) atomicAdd(&t.stats->evicted, n_evi);
+      if (n_rej) atomicAdd(&t.stats->rejected, n_rej);
+      if (n_adm != n_evi) atomicAdd(&t.stats->size, n_adm - n_evi);
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Dual mode (Algorithm 3).
+// Dual mode (Algorithm 3), as routing plus bucket ownership.
+//
+// Algorithm 3 sends an absent key to one of its two buckets: the less
+// occupied one while either has room (D1), else the one whose lowest rank is
+// lower, where it is admitted only if it outranks that minimum (D2).  The
+// bucket then runs Algorithm 2's placement.  Here each absent key is routed
+// by those rules on the bucket summaries (occupancy and lowest score, exact
+// as of the last pass over the bucket) and staged in the chosen bucket's
+// area; the bucket kernel of single mode then places every bucket's routed
+// keys with one warp per bucket (free slots first, then the top 128 by rank
+// (score, key) of entries and keys survive).  Keys that the first pass
+// displaces get one more routing with the summaries that pass left, and a
+// second pass.  Whatever the routing chose, a key that ends up absent lost to
+// a full bucket all of whose entries outrank it, which is the invariant the
+// tests check; the processing order, and so which keys win near the margin,
+// is this design's, as it is any parallel kernel's.
 // ---------------------------------------------------------------------------
-// Resident keys: update value (and score) in place; absent keys go to the
-// miss list.  One 8-lane tile per key.
-__global__ void __launch_bounds__(kThreads) dual_resident_kernel(
+
+// Algorithm 3's choice between b1 and b2 for a key of score s, from the
+// summaries.  Returns kNoBucket when the key cannot enter either bucket: both
+// full and s below both lowest scores (the summaries' lowest scores are never
+// above the true ones, so such a key would be rejected anyway).
+constexpr uint64_t kNoBucket = ~0ull;
+
+__device__ __forceinline__ uint64_t route_bucket(const TableView& t, uint64_t b1, uint64_t b2,
+                                                 uint64_t s) {
+  const BucketSummary x = t.summary[b1], y = t.summary[b2];
+  const uint32_t f1 = kSlots - min(x.count, static_cast<unsigned>(kSlots));
+  const uint32_t f2 = kSlots - min(y.count, static_cast<unsigned>(kSlots));
+  if (f1 || f2) return f2 > f1 ? b2 : b1;  // D1: the less occupied, ties to b1
+  const bool use2 = y.min_score < x.min_score;  // D2: the lower minimum
+  const uint64_t m = use2 ? y.min_score : x.min_score;
+  if (s < m) return kNoBucket;
+  return use2 ? b2 : b1;
+}
+
+// Stage key k (batch index i) in bucket target's area of the dual stage.
+// Keys are unique here (the batch was de-duplicated), so a CAS that loses
+// only means another key took the position.
+__device__ __forceinline__ void stage_routed(const TableView& t, const UpsertScratch& sc,
+                                             uint64_t target, uint64_t k, uint64_t h, uint64_t i,
+                                             uint64_t inc) {
+  const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
+  const uint64_t lo = area_start(target, S, B, sc.area_shift);
+  uint64_t p = stage_home(h, lo, area_start(target + 1, S, B, sc.area_shift) - lo) & mask;
+  // S >= 2n: a free position exists, so the probe ends within S steps
+  for (uint64_t tries = 0; tries < S; ++tries) {
+    if (atomicCAS(reinterpret_cast<unsigned long long*>(sc.stage_keys + p), kEmptyKey, k) ==
+        kEmptyKey)
+      break;
+    p = (p + 1) & mask;
+  }
+  sc.stage_idx[p] = static_cast<uint32_t>(i) + 1;
+  sc.stage_bkt[p] = static_cast<uint32_t>(target);
+  if (sc.stage_inc) sc.stage_inc[p] = inc;
+  sc.mark[target] = 1;
+}
+
+// Pass 1: resident keys update value (and score) in place; absent keys are
+// flagged in the dedup map (for the counts) and routed.  One 8-lane tile per
+// key.
+__global__ void __launch_bounds__(kThreads, 4) dual_route_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
     ScoreRule rule, bool vec) {
+  pdl_wait();
+  pdl_trigger();
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
@@ -833,12 +949,10 @@ __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
     if (ms == kNone) continue;
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
-    uint64_t b = bucket_of_hash(t, h);
-    int slot = tile_probe<true>(t, b, k, pat, sub, tmask);
-    if (slot < 0) {
-      b = bucket2_of(t, k, b);
-      slot = tile_probe<true>(t, b, k, pat, sub, tmask);
-    }
+    const uint64_t b1 = bucket_of_hash(t, h);
+    const uint64_t b2 = bucket2_of(t, k, b1);
+    uint64_t b = b1;
+    int slot = tile_probe_pair<true>(t, b1, b2, k, pat, sub, tmask, b);
     if (slot >= 0) {
       const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
       tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
@@ -847,172 +961,58 @@ __global__ void __launch_bounds__(kThreads) dual_resident_kernel(
         *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
         ++upd;
       }
-    } else if (sub == 0) {
-      sc.group[atomicAdd(sc.cursor + 1, 1u)] = static_cast<uint32_t>(i);
+    }
+    if (sub == 0) sc.absent[ms] = slot < 0 ? 1 : 0;  // for dual_count_kernel
+    if (slot < 0 && sub == 0) {
+      const uint64_t inc = entry_inc(sc, ms);
+      const uint64_t target = route_bucket(t, b1, b2, policy_score(rule, i, inc, false, 0));
+      if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
     }
   }
   warp_add(&t.stats->updated, upd);
 }
 
-__device__ __forceinline__ bool lock_bucket(uint32_t* lk) {
-  for (int it = 0; it < kSpinLimit; ++it) {
-    if (atomicCAS(lk, 0u, 1u) == 0u) {
-      __threadfence();
-      return true;
-    }
-    __nanosleep(it < 64 ? 32 : 256);
-  }
-  return false;
-}
-
-__device__ __forceinline__ void unlock_bucket(uint32_t* lk) {
-  __threadfence();
-  atomicExch(lk, 0u);
-}
-
-// Warp-wide arg-min of rank over one bucket's 128 slots; lane l holds slots
-// 4l..4l+3 in (s[q], k[q]).  Returns the slot index; (ms, mk) get its rank.
-__device__ __forceinline__ uint32_t warp_argmin(const uint64_t* s, const uint64_t* k, uint64_t& ms,
-                                                uint64_t& mk) {
-  const unsigned lane = lane_id();
-  uint64_t bs = s[0], bk = k[0];
-  uint32_t bslot = lane * 4;
-#pragma unroll
-  for (int q = 1; q < 4; ++q)
-    if (rank_less(s[q], k[q], bs, bk)) { bs = s[q]; bk = k[q]; bslot = lane * 4 + q; }
-  for (int off = 16; off > 0; off >>= 1) {
-    const uint64_t os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
-    const uint64_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-    const uint32_t osl = __shfl_xor_sync(0xFFFFFFFFu, bslot, off);
-    if (rank_less(os, ok, bs, bk)) { bs = os; bk = ok; bslot = osl; }
-  }
-  ms = bs; mk = bk;
-  return bslot;
-}
-
-// Absent keys: one warp per key, both candidate buckets locked.
-__global__ void __launch_bounds__(kThreads) dual_place_kernel(
-    TableView t, UpsertScratch sc, const uint64_t* keys, const float* values, ScoreRule rule,
-    bool vec) {
-  const unsigned lane = lane_id();
-  const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
-  const uint32_t nmiss = *(volatile uint32_t*)(sc.cursor + 1);
-  unsigned long long fills = 0, timeouts = 0;
-  for (uint64_t w = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < nmiss;
-       w += nwarps) {
-    const uint32_t i = sc.group[w];
+// Pass 2: the keys the first bucket pass displaced are routed again with the
+// summaries that pass left.  One thread per key.
+__global__ void __launch_bounds__(kThreads) dual_retry_kernel(TableView t, UpsertScratch sc,
+                                                              const uint64_t* keys,
+                                                              ScoreRule rule) {
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t nretry = sc.cursor[4];
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t w = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < nretry;
+       w += stride) {
+    const uint32_t i = sc.retry[w];
     const uint64_t k = keys[i];
     const uint64_t inc = sc.inc ? sc.inc[map_find(sc.map_keys, sc.map_size - 1, k)] : 0ull;
-    const uint64_t s = policy_score(rule, i, inc, false, 0);
     const uint64_t h = hash64(k);
     const uint64_t b1 = bucket_of_hash(t, h);
-    const uint64_t b2 = bucket2_of(t, k, b1);
-    const uint64_t lo = b1 < b2 ? b1 : b2, hi = b1 < b2 ? b2 : b1;
-    bool ok = true;
-    if (lane == 0) {
-      ok = lock_bucket(t.locks + lo);
-      if (ok && !lock_bucket(t.locks + hi)) {
-        unlock_bucket(t.locks + lo);
-        ok = false;
-      }
-      if (!ok) ++timeouts;
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) continue;
-    __threadfence();  // acquire side for every lane
-
-    uint64_t k1[4], k2[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      k1[q] = ld_cg_u64(key_at(t, b1 * kSlots + lane * 4 + q));
-      k2[q] = ld_cg_u64(key_at(t, b2 * kSlots + lane * 4 + q));
-    }
-    int f1 = -1, f2 = -1, c1 = 0, c2 = 0;
-#pragma unroll
-    for (int q = 3; q >= 0; --q) {
-      if (k1[q] == kEmptyKey) { f1 = q; ++c1; }
-      if (k2[q] == kEmptyKey) { f2 = q; ++c2; }
-    }
-    int free1 = c1, free2 = c2;
-    for (int off = 16; off > 0; off >>= 1) {
-      free1 += __shfl_xor_sync(0xFFFFFFFFu, free1, off);
-      free2 += __shfl_xor_sync(0xFFFFFFFFu, free2, off);
-    }
-    uint64_t tb = 0;
-    int tslot = -1;
-    if (free1 > 0 || free2 > 0) {
-      // Phase D1: the less occupied bucket (more free slots), ties to b1.
-      const bool use2 = free2 > free1;
-      tb = use2 ? b2 : b1;
-      const unsigned fm = __ballot_sync(0xFFFFFFFFu, (use2 ? f2 : f1) >= 0);
-      const int fl = __ffs(fm) - 1;
-      const int fq = __shfl_sync(0xFFFFFFFFu, use2 ? f2 : f1, fl);
-      tslot = fl * 4 + fq;
-      ++fills;
-    } else {
-      // Phase D2: compare the two bucket minima; admission against the lower.
-      uint64_t s1[4], s2[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        s1[q] = ld_cg_u64(score_at(t, b1 * kSlots + lane * 4 + q));
-        s2[q] = ld_cg_u64(score_at(t, b2 * kSlots + lane * 4 + q));
-      }
-      uint64_t ms1, mk1, ms2, mk2;
-      const uint32_t m1 = warp_argmin(s1, k1, ms1, mk1);
-      const uint32_t m2 = warp_argmin(s2, k2, ms2, mk2);
-      const bool use2 = rank_less(ms2, mk2, ms1, mk1);
-      const uint64_t ms = use2 ? ms2 : ms1, mk = use2 ? mk2 : mk1;
-      if (rank_less(ms, mk, s, k)) {
-        tb = use2 ? b2 : b1;
-        tslot = static_cast<int>(use2 ? m2 : m1);
-      }
-    }
-    if (tslot >= 0) {
-      const uint64_t row = tb * kSlots + static_cast<uint64_t>(tslot);
-      if (lane == 0) {
-        *key_at(t, row) = k;
-        *score_at(t, row) = s;
-        t.digests[row] = static_cast<uint8_t>(digest_of_hash(h));
-      }
-      float* dst = row_ptr(t, row);
-      const float* src = values + static_cast<uint64_t>(i) * t.dim;
-      if (vec) {
-        for (uint32_t c = lane; c < (t.dim >> 2); c += 32)
-          st_stream_v4(dst + 4 * c, ld_stream_v4(src + 4 * c));
-      } else {
-        for (uint32_t c = lane; c < t.dim; c += 32) dst[c] = src[c];
-      }
-    }
-    __threadfence();  // release side: every lane's writes before the unlock
-    __syncwarp();
-    if (lane == 0) {
-      unlock_bucket(t.locks + hi);
-      unlock_bucket(t.locks + lo);
-    }
-  }
-  if (lane == 0) {
-    if (fills) atomicAdd(&t.stats->fills, fills);
-    if (timeouts) atomicAdd(&t.stats->timeouts, timeouts);
+    const uint64_t target =
+        route_bucket(t, b1, bucket2_of(t, k, b1), policy_score(rule, i, inc, false, 0));
+    if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
   }
 }
 
 // After placement: count admitted (resident) vs rejected absent keys.
 __global__ void __launch_bounds__(kThreads) dual_count_kernel(TableView t, UpsertScratch sc,
-                                                              const uint64_t* keys) {
+                                                              uint64_t n, const uint64_t* keys) {
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tmask = 0xFFu << (lane & 24u);
   const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
-  const uint32_t nmiss = sc.cursor[1];
   unsigned long long adm = 0, rej = 0;
-  for (uint64_t w = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; w < nmiss;
-       w += tiles) {
-    const uint64_t k = keys[sc.group[w]];
+  for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
+       i += tiles) {
+    const uint64_t k = keys[i];
+    if (is_reserved(k)) continue;
+    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    if (ms == kNone || !sc.absent[ms]) continue;  // a duplicate, or resident before the call
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
     const uint64_t b1 = bucket_of_hash(t, h);
-    int slot = tile_probe<true>(t, b1, k, pat, sub, tmask);
-    if (slot < 0) slot = tile_probe<true>(t, bucket2_of(t, k, b1), k, pat, sub, tmask);
+    uint64_t b;
+    const int slot = tile_probe_pair<true>(t, b1, bucket2_of(t, k, b1), k, pat, sub, tmask, b);
     if (sub == 0) {
       if (slot >= 0) ++adm;
       else ++rej;
@@ -1106,6 +1106,7 @@ __global__ void __launch_bounds__(kThreads) erase_kernel(TableView t, uint64_t n
       // Duplicates of k in the batch race here; exactly one CAS wins.
       if (atomicCAS(reinterpret_cast<unsigned long long*>(key_at(t, row)), k, kEmptyKey) == k) {
         t.digests[row] = 0;
+        if (t.summary) atomicSub(&t.summary[b].count, 1u);  // dual mode: keep occupancy exact
         ++erased;
       }
     }
@@ -1149,8 +1150,10 @@ size_t upsert_scratch_bytes(uint64_t n, uint64_t num_buckets, ScratchKind kind, 
   const uint64_t m = stage_entries(n);
   size_t bytes = align256(m * 8) + align256(m * 4) + align256(64);
   if (kind == ScratchKind::kSingleUpsert) bytes += align256(num_buckets);
-  if (kind == ScratchKind::kDualUpsert) bytes += align256(n * 4);
-  if (lfu) bytes += align256(m * 8);
+  if (kind == ScratchKind::kDualUpsert)
+    bytes += align256(m) + align256(n * 4) + align256(m * 8) + 2 * align256(m * 4) +
+             align256(num_buckets);
+  if (lfu) bytes += align256(m * 8) * (kind == ScratchKind::kDualUpsert ? 2 : 1);
   return bytes;
 }
 
@@ -1159,6 +1162,11 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
   UpsertScratch s{};
   const uint64_t m = stage_entries(n);
   char* p = static_cast<char*>(base);
+  auto take = [&](size_t bytes) {
+    char* q = p;
+    p += align256(bytes);
+    return q;
+  };
   s.map_size = static_cast<uint32_t>(m);
   s.area_shift = kNoShift;
   if ((num_buckets & (num_buckets - 1)) == 0) {
@@ -1167,18 +1175,26 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
     while ((1ull << lm) < m) ++lm;
     s.area_shift = lm - lb;
   }
-  s.map_keys = reinterpret_cast<uint64_t*>(p); p += align256(m * 8);
-  s.map_idx = reinterpret_cast<uint32_t*>(p); p += align256(m * 4);
-  s.cursor = reinterpret_cast<uint32_t*>(p); p += align256(64);
+  s.map_keys = reinterpret_cast<uint64_t*>(take(m * 8));
+  s.map_idx = reinterpret_cast<uint32_t*>(take(m * 4));
+  s.cursor = reinterpret_cast<uint32_t*>(take(64));
   if (kind == ScratchKind::kSingleUpsert) {
-    s.mark = reinterpret_cast<uint8_t*>(p); p += align256(num_buckets);
+    s.mark = reinterpret_cast<uint8_t*>(take(num_buckets));
     if (n >= 2 * num_buckets) s.mark = nullptr;  // dense batch: no marks
   }
+  if (lfu) s.inc = reinterpret_cast<uint64_t*>(take(m * 8));
   if (kind == ScratchKind::kDualUpsert) {
-    s.group = reinterpret_cast<uint32_t*>(p); p += align256(n * 4);
-  }
-  if (lfu) {
-    s.inc = reinterpret_cast<uint64_t*>(p); p += align256(m * 8);
+    s.absent = reinterpret_cast<uint8_t*>(take(m));
+    s.retry = reinterpret_cast<uint32_t*>(take(n * 4));
+    s.stage_keys = reinterpret_cast<uint64_t*>(take(m * 8));
+    s.stage_idx = reinterpret_cast<uint32_t*>(take(m * 4));
+    s.stage_bkt = reinterpret_cast<uint32_t*>(take(m * 4));
+    s.mark = reinterpret_cast<uint8_t*>(take(num_buckets));
+    if (lfu) s.stage_inc = reinterpret_cast<uint64_t*>(take(m * 8));
+  } else {  // the single-mode stage is the dedup map itself
+    s.stage_keys = s.map_keys;
+    s.stage_idx = s.map_idx;
+    s.stage_inc = s.inc;
   }
   return s;
 }
@@ -1186,31 +1202,70 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
 namespace {
 
 // One launch clears every scratch array of a call: the map keys to EMPTY, the
-// map indices (and LFU sums) to 0, the counters and the bucket marks to 0.
+// map indices (and LFU sums) to 0, the counters and the bucket marks to 0,
+// and in dual mode the routed stage's keys to EMPTY.  stage_only clears just
+// the routed stage and the marks (between the two dual-mode passes).
 // map_size is a power of two >= 64, and every array starts 256-byte aligned.
 __global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s,
-                                                                 uint64_t mark_bytes) {
+                                                                 uint64_t mark_bytes,
+                                                                 bool stage_only) {
   pdl_wait();
   pdl_trigger();
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   const uint64_t pairs = s.map_size / 2;
+  const bool routed = s.stage_keys != s.map_keys;
   for (uint64_t i = tid; i < pairs; i += stride) {
-    reinterpret_cast<ulonglong2*>(s.map_keys)[i] = make_ulonglong2(kEmptyKey, kEmptyKey);
-    reinterpret_cast<uint2*>(s.map_idx)[i] = make_uint2(0u, 0u);
-    if (s.inc) reinterpret_cast<ulonglong2*>(s.inc)[i] = make_ulonglong2(0ull, 0ull);
+    if (!stage_only) {
+      reinterpret_cast<ulonglong2*>(s.map_keys)[i] = make_ulonglong2(kEmptyKey, kEmptyKey);
+      reinterpret_cast<uint2*>(s.map_idx)[i] = make_uint2(0u, 0u);
+      if (s.inc) reinterpret_cast<ulonglong2*>(s.inc)[i] = make_ulonglong2(0ull, 0ull);
+    }
+    if (routed) reinterpret_cast<ulonglong2*>(s.stage_keys)[i] = make_ulonglong2(kEmptyKey, kEmptyKey);
   }
-  if (tid < 16) s.cursor[tid] = 0u;
+  if (!stage_only && tid < 16) s.cursor[tid] = 0u;
   if (s.mark)
     for (uint64_t i = tid; i < mark_bytes; i += stride) s.mark[i] = 0;
+}
+
+// One bucket pass (single or dual mode).  Non-LFU rules become one score per
+// call (the clock, folded with the epoch) unless the caller gives scores.
+template <bool kDual>
+cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
+                               const float* values, const ScoreRule& rule, bool vec,
+                               cudaStream_t st, const UpsertExtra& ex) {
+  const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
+  cudaError_t e = cudaSuccess;
+  if (rule.lfu()) {
+    const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kThreads / 32) : 0;
+    if (smem)
+      e = cudaFuncSetAttribute(upsert_single_kernel<true, kDual>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_chained(upsert_single_kernel<true, kDual>, grid, kThreads, smem, st, t, s, keys,
+                          values, rule, vec, ex);
+  }
+  ScoreRule r = rule;
+  if (rule.policy != kCustomized) r.in = nullptr;
+  if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
+  r.policy = kCustomized;
+  const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kThreads / 32) : 0;
+  if (smem)
+    e = cudaFuncSetAttribute(upsert_single_kernel<false, kDual>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_chained(upsert_single_kernel<false, kDual>, grid, kThreads, smem, st, t, s, keys,
+                        values, r, vec, ex);
 }
 
 }  // namespace
 
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
                                  cudaStream_t st) {
-  const uint64_t mark_bytes = kind == ScratchKind::kSingleUpsert && s.mark ? num_buckets : 0;
-  return launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, 0, st, s, mark_bytes);
+  const uint64_t mark_bytes = s.mark ? num_buckets : 0;
+  (void)kind;
+  return launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, 0, st, s,
+                        mark_bytes, false);
 }
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,
@@ -1219,43 +1274,31 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   if (n == 0) return cudaSuccess;
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
   const uint64_t* inc_in = rule.lfu() ? rule.in : nullptr;
+  cudaError_t e = cudaSuccess;
   if (!t.dual) {
-    cudaError_t e = launch_chained(stage_kernel,
-                                   grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread),
-                                   kThreads, 0, st, t, s, n, keys, inc_in);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
-    if (rule.lfu()) {
-      const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kThreads / 32) : 0;
-      if (smem) e = cudaFuncSetAttribute(upsert_single_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-      e = launch_chained(upsert_single_kernel<true>, grid, kThreads, smem, st, t, s, keys, values,
-                         rule, vec, ex);
-      if (e != cudaSuccess) return e;
-    } else {
-      // one score per call unless the caller gives scores (kCustomized)
-      ScoreRule r = rule;
-      if (rule.policy != kCustomized) r.in = nullptr;
-      if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
-      r.policy = kCustomized;
-      const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kThreads / 32) : 0;
-      if (smem) e = cudaFuncSetAttribute(upsert_single_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-      e = launch_chained(upsert_single_kernel<false>, grid, kThreads, smem, st, t, s, keys, values,
-                         r, vec, ex);
-      if (e != cudaSuccess) return e;
-    }
-  } else {
-    dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, inc_in, t.stats);
-    dual_resident_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, rule, vec);
-    dual_place_kernel<<<grid_for(n * 32), kThreads, 0, st>>>(t, s, keys, values, rule, vec);
-    dual_count_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, keys);
-    dual_finish_kernel<<<1, 1, 0, st>>>(t, s);
+    e = launch_chained(stage_kernel, grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread),
+                       kThreads, 0, st, t, s, n, keys, inc_in);
+    if (e == cudaSuccess) e = launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, ex);
+    return e;
   }
+  // Dual mode: de-duplicate; update residents and route absent keys; place
+  // them bucket by bucket; route the displaced ones once more and place
+  // them; count.
+  dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, inc_in, t.stats);
+  e = launch_chained(dual_route_kernel, grid_for(n * 8), kThreads, 0, st, t, s, n, keys, values,
+                     rule, vec);
+  UpsertExtra first = ex;
+  first.collect_retry = true;
+  if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, first);
+  if (e == cudaSuccess)
+    e = launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, 0, st, s,
+                       t.num_buckets, true);
+  if (e == cudaSuccess)
+    e = launch_chained(dual_retry_kernel, grid_for(n), kThreads, 0, st, t, s, keys, rule);
+  if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, ex);
+  if (e != cudaSuccess) return e;
+  dual_count_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys);
+  dual_finish_kernel<<<1, 1, 0, st>>>(t, s);
   return cudaGetLastError();
 }
 

@@ -23,8 +23,14 @@
  * keys already resident are updated first, then the absent keys are placed;
  * in single mode the result is therefore a pure function of the table and the
  * batch (bucket b ends up with the 128 highest-ranked of its residents and of
- * the absent keys hashed to it).  In dual mode the placement of absent keys
- * depends on the order the GPU processes them.
+ * the absent keys hashed to it).  In dual mode each absent key is routed to
+ * one of its buckets by Algorithm 3's rules applied to per-bucket summaries
+ * (occupancy and lowest score as of the bucket's last upsert pass), each
+ * bucket then keeps the highest-ranked of its entries and its routed keys,
+ * and the keys displaced by that pass are routed once more with the updated
+ * summaries; which keys win near the margin depends on that processing
+ * order, but a key that ends up absent always lost to a full bucket all of
+ * whose entries outrank it.
  *
  * Memory: all pointer arguments except the `*_host` ones are device pointers
  * (or pointers the device can dereference: mapped or managed host memory).
@@ -142,7 +148,8 @@ hkv_status hkv_find(hkv_table* table, uint64_t n, const uint64_t* keys, float* v
  * its bucket (dual mode: the less occupied candidate, ties to b1); when the
  * bucket is full (dual: both full) it replaces the lowest-ranked entry of the
  * bucket (dual: of the candidate whose lowest rank is lower) if it ranks
- * higher than that entry, else it is rejected.
+ * higher than that entry, else it is rejected.  Dual mode applies these rules
+ * batch-wise as described under "Batches".
  *  scores  per-key scores (LFU policies: increments) or NULL; the score an
  *          entry receives follows the table's policy (see "Score
  *          policies"); under HKV_POLICY_CUSTOMIZED, NULL gives every key of
@@ -218,8 +225,9 @@ hkv_status hkv_export(hkv_table* table, uint64_t slot_begin, uint64_t slot_end, 
 
 /* Cumulative counts since creation, read synchronously (waits for the
  * table's outstanding work).  reserved_keys: input keys skipped because they
- * were reserved sentinels.  timeouts: keys abandoned after a bounded wait on
- * a bucket lock (dual mode); nonzero means those keys were not applied.
+ * were reserved sentinels.  timeouts: bounded device-side waits that ran out
+ * (none in the default build; the pipelined measurement build counts a bucket
+ * copy that did not arrive in time, then loads that bucket directly).
  * Returns HKV_ERR_TIMEOUT when timeouts > 0, else HKV_ERR_RESERVED_KEY when
  * reserved_keys > 0, else HKV_OK; the counts are written in every case. */
 hkv_status hkv_get_error_counts(hkv_table* table, uint64_t* reserved_keys_host,
@@ -263,10 +271,10 @@ hkv_status hkv_set_epoch(hkv_table* table, uint32_t epoch);
  * the device).  It calls no allocation routine.
  *  - Limit: the batch's working memory must fit the array, i.e.
  *      a(8M) + a(4M) + 256 + a(B) bytes in single mode and
- *      a(8M) + a(4M) + 256 + a(4n) bytes in dual mode,
- *    plus a(8M) under the LFU policies, with M the smallest power of two
- *    >= max(64, 2n), B the bucket count and a(x) = x rounded up to a
- *    multiple of 256.  Larger batches return HKV_ERR_INVALID and enqueue
+ *      2 a(8M) + 3 a(4M) + 256 + 2 a(4n) + a(B) bytes in dual mode,
+ *    plus a(8M) under the LFU policies (2 a(8M) in dual mode), with M the
+ *    smallest power of two >= max(64, 2n), B the bucket count and a(x) = x
+ *    rounded up to a multiple of 256.  Larger batches return HKV_ERR_INVALID and enqueue
  *    nothing (split them, or use hkv_insert_or_assign).  Single mode takes
  *    up to 2^20 keys per call (2^19 under the LFU policies) for tables of up
  *    to 2^23 buckets.
