@@ -108,11 +108,15 @@ def upsert_access_floor(n, dim, rows_written, buckets_touched, rates, hbm_gbs):
 
 # DRAM bytes (read + write) of one launch, from an ncu capture of the timed
 # region of `python bench.py --skip-sweep --no-cpu-baseline --steps 3
-# --warmup 3` (profiles/find_kernel_c2.md), valid only while the kernel's
-# sources are the ones captured (sha256 prefix over the listed files).
+# --warmup 3` (profiles/find_kernel_c2.md, profiles/upsert_kernels_c2.md),
+# valid only while the kernel's sources are the ones captured (sha256 prefix
+# over the listed files).
 NCU_TRAFFIC = {
-    "find_kernel": {"bytes": 164763648 + 69147136, "sources": ("find.cu", "common.cuh", "launch.h"),
-                    "sha256": "b8d4766bd92480c0"},
+    "find_kernel": {"bytes": 164755712 + 69267968, "sources": ("find.cu", "common.cuh", "launch.h"),
+                    "sha256": "2f71ef7c08587846"},
+    "upsert_single_kernel": {"bytes": 180340736 + 60790016,
+                             "sources": ("upsert.cu", "common.cuh", "launch.h"),
+                             "sha256": "2420e2e798aebd03"},
 }
 
 
@@ -360,8 +364,10 @@ def run_gpu(args):
                  "frac": fb / f_avg / 1e9 / peak, "traffic": ncu_traffic("find_kernel"),
                  "kernel": "find_kernel",
                  "bytes_per_launch": fb, "avg_launch_s": f_avg, "peak_kind": peak_kind}
+    up_traffic = ncu_traffic("upsert_single_kernel")
     up_roof = {"bound": "hbm", "achieved": ub / u_avg / 1e9, "peak": peak, "unit": "GB/s",
-               "frac": ub / u_avg / 1e9 / peak, "traffic": None,
+               "frac": ub / u_avg / 1e9 / peak,
+               "traffic": None if up_traffic is None else {"upsert_single_kernel": up_traffic},
                "kernel": "insert_or_assign call (stage_kernel + upsert_single_kernel)",
                "bytes_per_launch": ub, "avg_launch_s": u_avg, "peak_kind": peak_kind}
     dominant = find_roof
