@@ -271,7 +271,7 @@ hkv_status hkv_set_epoch(hkv_table* table, uint32_t epoch);
  * the device).  It calls no allocation routine.
  *  - Limit: the batch's working memory must fit the array, i.e.
  *      a(8M) + a(4M) + 256 + a(B) bytes in single mode and
- *      2 a(8M) + 3 a(4M) + 256 + 2 a(4n) + a(B) bytes in dual mode,
+ *      2 a(8M) + 3 a(4M) + a(M) + 256 + a(4n) + a(B) bytes in dual mode,
  *    plus a(8M) under the LFU policies (2 a(8M) in dual mode), with M the
  *    smallest power of two >= max(64, 2n), B the bucket count and a(x) = x
  *    rounded up to a multiple of 256.  Larger batches return HKV_ERR_INVALID and enqueue
