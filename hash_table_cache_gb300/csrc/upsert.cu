@@ -638,10 +638,16 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
       for (uint32_t x = 0; x < E; ++x) {
         const uint32_t m =
             __reduce_min_sync(0xFFFFFFFFu, min(min(min(rf[0], rf[1]), min(rf[2], rf[3])), mf));
+        // branch-free: every element equal to the minimum leaves
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (rf[q] == m) { rf[q] = kGone; rem |= 1u << q; }
-        if (mf == m) { mf = kGone; pending = false; }
+        for (int q = 0; q < 4; ++q) {
+          const bool out_q = rf[q] == m;
+          rf[q] = out_q ? kGone : rf[q];
+          rem |= out_q ? (1u << q) : 0u;
+        }
+        const bool out_m = mf == m;
+        mf = out_m ? kGone : mf;
+        pending = pending && !out_m;
       }
       const uint32_t out = __popc(rem) + ((pending0 && !pending) ? 1u : 0u);
       if (__reduce_add_sync(0xFFFFFFFFu, out) != E) {
@@ -816,10 +822,9 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
 
     // Phase C: write back the lane's changed slots and digest bytes, then
     // copy the value rows of the final occupants.
-    uint32_t dm = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (st.occ[lane * 4 + q] != kNone) dm |= 1u << q;
+    const uint4 oc = *reinterpret_cast<const uint4*>(&st.occ[lane * 4]);
+    const uint32_t dm = (oc.x != kNone ? 1u : 0u) | (oc.y != kNone ? 2u : 0u) |
+                        (oc.z != kNone ? 4u : 0u) | (oc.w != kNone ? 8u : 0u);
     if (dm) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -836,7 +841,10 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     for (int q = 0; q < 4; ++q)
       if (dm & (1u << q)) st.list[pos++] = static_cast<uint8_t>(lane * 4 + q);
     __syncwarp();
-    // four rows per tile per pass, loads in flight together
+    // four rows per tile per pass, loads in flight together; a bucket's rows
+    // are contiguous and all in HBM or all in host memory (the split falls
+    // on a bucket boundary)
+    float* const rows = row_ptr(t, b * kSlots);
     for (uint32_t p0 = lane >> 3; p0 < total; p0 += 16) {
       float* dst[4];
       const float* src[4];
@@ -846,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
         const uint32_t p = p0 + 4 * r;
         ok[r] = p < total;
         const uint32_t slot = ok[r] ? st.list[p] : 0;
-        dst[r] = row_ptr(t, b * kSlots + slot);
+        dst[r] = rows + slot * t.dim;
         src[r] = values_in + static_cast<uint64_t>(ok[r] ? st.occ[slot] : 0) * t.dim;
       }
       tile_copy_rows<4>(dst, src, ok, t.dim, sub, vec);
