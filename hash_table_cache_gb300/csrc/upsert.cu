@@ -730,10 +730,12 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
     };
 
     auto build_free_list = [&]() {
-      uint32_t fm = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (st.key[lane * 4 + q] == kEmptyKey) fm |= 1u << q;
+      // a free slot is a zero digest byte (phase A changes no digest)
+      const uint32_t fm = byte_eq_mask4(dw, 0u);
+      if (!__any_sync(0xFFFFFFFFu, fm != 0)) {  // full bucket: nothing to list
+        nfree = 0;
+        return;
+      }
       uint32_t pos = prefix_small(__popc(fm), nfree);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
