@@ -460,9 +460,34 @@ def run_gpu(args):
         e_total = a.elapsed_time(b) * 1e-3
         bi = hk[0].numel() * 8 + hv[0].numel() * 4 + hq[0].numel() * 8
         bo = hvo[0].numel() * 4 + hfo[0].numel() + hso[0].numel() * 8
+        # The host link alone: the same uploads and downloads with no table
+        # work between them, both directions on their own streams.
+        torch.cuda.synchronize()
+        a.record(stream)
+        up_s.wait_event(a)
+        dn_s.wait_event(a)
+        for s in range(ne):
+            i = s % 2
+            with torch.cuda.stream(up_s):
+                dk_[i].copy_(hk[i], non_blocking=True)
+                dv_[i].copy_(hv[i], non_blocking=True)
+                dq_[i].copy_(hq[i], non_blocking=True)
+            with torch.cuda.stream(dn_s):
+                hvo[i].copy_(ov_[i], non_blocking=True)
+                hfo[i].copy_(of_[i], non_blocking=True)
+                hso[i].copy_(os_[i], non_blocking=True)
+        for s_ in (up_s, dn_s):
+            x = torch.cuda.Event()
+            x.record(s_)
+            stream.wait_event(x)
+        b.record(stream)
+        b.synchronize()
+        link_total = a.elapsed_time(b) * 1e-3
         e2e = {"value": 2 * BATCH * ne * world / e_total / 1e9, "unit": "B-KV/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "steps": ne, "overlap": "uploads and downloads on their own streams, double buffered"}
+               "steps": ne, "overlap": "uploads and downloads on their own streams, double buffered",
+               "link_only_s_per_step": link_total / ne,
+               "frac_of_link_bound": link_total / e_total}
     t.close()
 
     cpu = None
