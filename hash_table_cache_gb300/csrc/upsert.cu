@@ -37,9 +37,13 @@ namespace hkv {
 namespace {
 
 constexpr int kThreads = 256;
+#ifndef HKV_BUCKET_THREADS
+#define HKV_BUCKET_THREADS 256
+#endif
 #ifndef HKV_UPSERT_MIN_BLOCKS
 #define HKV_UPSERT_MIN_BLOCKS 3
 #endif
+constexpr int kBucketThreads = HKV_BUCKET_THREADS;  // bucket kernel block size
 #ifndef HKV_UPSERT_PIPELINE
 #define HKV_UPSERT_PIPELINE 0
 #endif
@@ -372,7 +376,7 @@ constexpr int kCopyWaitLimit = 1 << 14;
 #endif
 
 template <bool kLfu, bool kDual>
-__global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
+__global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
     ScoreRule rule, bool vec, UpsertExtra ex) {
   (void)keys_in;  // entry keys come from the stage
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BucketStage<kLfu>* stage_all = reinterpret_cast<BucketStage<kLfu>*>(smem_raw);
 #else
-  __shared__ BucketStage<kLfu> stage_all[kThreads / 32];
+  __shared__ BucketStage<kLfu> stage_all[kBucketThreads / 32];
 #endif
   pdl_wait();
   pdl_trigger();
@@ -1244,27 +1248,30 @@ template <bool kDual>
 cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
                                const float* values, const ScoreRule& rule, bool vec,
                                cudaStream_t st, const UpsertExtra& ex) {
-  const unsigned grid = grid_for(t.num_buckets * 32, HKV_UPSERT_MIN_BLOCKS);
+  // one warp per bucket, at most one wave of resident blocks
+  uint64_t blocks = (t.num_buckets * 32 + kBucketThreads - 1) / kBucketThreads;
+  const uint64_t cap = static_cast<uint64_t>(sm_count()) * HKV_UPSERT_MIN_BLOCKS;
+  const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
   cudaError_t e = cudaSuccess;
   if (rule.lfu()) {
-    const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kThreads / 32) : 0;
+    const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kBucketThreads / 32) : 0;
     if (smem)
       e = cudaFuncSetAttribute(upsert_single_kernel<true, kDual>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_chained(upsert_single_kernel<true, kDual>, grid, kThreads, smem, st, t, s, keys,
+    return launch_chained(upsert_single_kernel<true, kDual>, grid, kBucketThreads, smem, st, t, s, keys,
                           values, rule, vec, ex);
   }
   ScoreRule r = rule;
   if (rule.policy != kCustomized) r.in = nullptr;
   if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
   r.policy = kCustomized;
-  const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kThreads / 32) : 0;
+  const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kBucketThreads / 32) : 0;
   if (smem)
     e = cudaFuncSetAttribute(upsert_single_kernel<false, kDual>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_chained(upsert_single_kernel<false, kDual>, grid, kThreads, smem, st, t, s, keys,
+  return launch_chained(upsert_single_kernel<false, kDual>, grid, kBucketThreads, smem, st, t, s, keys,
                         values, r, vec, ex);
 }
 
