@@ -148,6 +148,14 @@ __device__ __forceinline__ uint64_t stage_home(uint64_t h, uint64_t lo, uint64_t
 #endif
 constexpr int kStageKeysPerThread = HKV_STAGE_KEYS_PER_THREAD;
 
+// kWarpDedup: lanes of a warp holding the same key let only the highest
+// (largest batch index) enter the stage, so a key repeated many times in a
+// skewed batch costs fewer atomics on its one address (not under the LFU
+// policies, where every occurrence adds its own increment).  Used for sparse
+// batches (at most 4 keys per bucket), where skewed workloads over large
+// tables live; dense batches run the plain kernel, which keeps more blocks
+// resident.
+template <bool kWarpDedup>
 __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScratch sc, uint64_t n,
                                                          const uint64_t* keys,
                                                          const uint64_t* inc_in) {
@@ -157,8 +165,9 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
   const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   unsigned long long reserved = 0;
-  for (uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
-       i0 += stride * U) {
+  // (with kWarpDedup the trip count is warp-uniform: whole warps iterate)
+  for (uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       (kWarpDedup ? i0 - lane_id() : i0) < n; i0 += stride * U) {
     uint64_t k[U], pos[U], b[U];
     bool v[U];
 #pragma unroll
@@ -170,6 +179,9 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
         ++reserved;
         v[u] = false;
       }
+      if (kWarpDedup && !sc.inc &&
+          (__match_any_sync(0xFFFFFFFFu, k[u]) >> lane_id()) > 1u)
+        v[u] = false;
       const uint64_t h = hash64(k[u]);
       b[u] = bucket_of_hash(t, h);
       const uint64_t lo = area_start(b[u], S, B, sc.area_shift);
@@ -1293,8 +1305,10 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   const uint64_t* inc_in = rule.lfu() ? rule.in : nullptr;
   cudaError_t e = cudaSuccess;
   if (!t.dual) {
-    e = launch_chained(stage_kernel, grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread),
-                       kThreads, 0, st, t, s, n, keys, inc_in);
+    const unsigned sg = grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread);
+    const bool sparse = n <= 4 * t.num_buckets;  // a few keys per bucket
+    e = sparse ? launch_chained(stage_kernel<true>, sg, kThreads, 0, st, t, s, n, keys, inc_in)
+               : launch_chained(stage_kernel<false>, sg, kThreads, 0, st, t, s, n, keys, inc_in);
     if (e == cudaSuccess) e = launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, ex);
     return e;
   }
