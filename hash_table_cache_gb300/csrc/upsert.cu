@@ -64,14 +64,27 @@ __device__ __forceinline__ uint32_t map_find(const uint64_t* mkeys, uint32_t mas
   return kNone;
 }
 
-// Map entry of `key` when batch index i is its last occurrence, else kNone.
-__device__ __forceinline__ uint32_t last_occurrence_slot(const UpsertScratch& sc, uint64_t key,
-                                                         uint64_t i) {
+// Map entry of `key` when batch index i is its last occurrence, else kNone,
+// looked up by the 8 lanes of a tile: they read 8 consecutive probe
+// positions at once, one round trip per 8 positions.
+__device__ __forceinline__ uint32_t tile_last_occurrence(const UpsertScratch& sc, uint64_t key,
+                                                         uint64_t i, unsigned sub,
+                                                         unsigned tmask) {
   const uint32_t mask = sc.map_size - 1;
-  const uint32_t s = map_find(sc.map_keys, mask, key);
-  const bool last =
-      s != kNone && sc.map_keys[s] == key && sc.map_idx[s] == static_cast<uint32_t>(i) + 1;
-  return last ? s : kNone;
+  const uint32_t home = map_home(key, mask);
+  const unsigned first_lane = lane_id() & 24u;
+  for (uint32_t p0 = 0; p0 <= mask; p0 += 8) {
+    const uint64_t v = sc.map_keys[(home + p0 + sub) & mask];
+    const unsigned hit = (__ballot_sync(tmask, v == key) & tmask) >> first_lane;
+    const unsigned emp = (__ballot_sync(tmask, v == kEmptyKey) & tmask) >> first_lane;
+    if (hit | emp) {  // the first position holding the key or free ends the probe
+      const int f = __ffs(hit | emp) - 1;
+      if (!((hit >> f) & 1u)) return kNone;
+      const uint32_t slot = (home + p0 + static_cast<uint32_t>(f)) & mask;
+      return sc.map_idx[slot] == static_cast<uint32_t>(i) + 1 ? slot : kNone;
+    }
+  }
+  return kNone;
 }
 
 // Summed increment of a deduplicated entry (LFU policies; 0 otherwise).
@@ -971,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 4) dual_route_kernel(
        i += tiles) {
     const uint64_t k = keys[i];
     if (is_reserved(k)) continue;
-    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
     if (ms == kNone) continue;
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
@@ -1032,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads) dual_count_kernel(TableView t, Upser
        i += tiles) {
     const uint64_t k = keys[i];
     if (is_reserved(k)) continue;
-    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
     if (ms == kNone || !sc.absent[ms]) continue;  // a duplicate, or resident before the call
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
@@ -1081,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScr
        i += tiles) {
     const uint64_t k = keys[i];
     if (is_reserved(k)) continue;
-    const uint32_t ms = last_occurrence_slot(sc, k, i);
+    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
     if (ms == kNone) continue;
     const uint64_t h = hash64(k);
     const uint32_t pat = digest_of_hash(h) * 0x01010101u;
