@@ -296,6 +296,18 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
     }
   }
   if (e == cudaSuccess) e = hkv::launch_clear_table(v, t->aux);
+  if (e == cudaSuccess) {
+    // Grow the scratch pool once now, to what an insert_or_assign of
+    // min(capacity, 2^20) keys needs, so the first batches do not pay for
+    // the pool's first allocation (the pool keeps what it holds).
+    const uint64_t n_warm = capacity < (1ull << 20) ? capacity : (1ull << 20);
+    const hkv::ScratchKind kind = dual ? hkv::ScratchKind::kDualUpsert
+                                       : hkv::ScratchKind::kSingleUpsert;
+    void* warm = nullptr;
+    e = cudaMallocFromPoolAsync(&warm, hkv::upsert_scratch_bytes(n_warm, nb, kind, lfu_policy(t)),
+                                t->pool, t->aux);
+    if (e == cudaSuccess) e = cudaFreeAsync(warm, t->aux);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(t->aux);
   if (e != cudaSuccess) {
     cudaGetLastError();
