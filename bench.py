@@ -515,7 +515,8 @@ def run_gpu(args):
         "lambda_sweep": {str(k): v for k, v in sweep.items()},
         "api_at_load_factor_1": api,
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
-        "gpu_launches": args.steps * 3,  # stage_kernel + upsert_single_kernel + find_kernel
+        # clear_scratch_kernel + stage_kernel + upsert_single_kernel + find_kernel
+        "gpu_launches": args.steps * 4,
     }
     print(json.dumps(line))
 
@@ -597,7 +598,7 @@ def run_other(args):
             if s >= args.warmup:
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(2 * n)
-        launches = 3
+        launches = 4  # clear, stage, bucket, find
     elif cfg == "c3":
         cap, dim, n = 1 << 26, 64, 1 << 20
         t = hkv.HashTable(cap, dim)
@@ -619,7 +620,7 @@ def run_other(args):
             if s >= args.warmup:
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(2 * n)
-        launches = 3
+        launches = 4  # clear, stage, bucket, find
     elif cfg == "c4":
         cap, dim, n = 1 << 26, 128, 1 << 20
         t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_DUAL)
@@ -643,7 +644,9 @@ def run_other(args):
             if s >= args.warmup:
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(2 * n)
-        launches = 7
+        # clear, dedup, route, bucket pass, clear, retry, bucket pass, count,
+        # finish, find
+        launches = 10
     elif cfg == "c5":
         cap, dim, n = 1 << 28, 64, 1 << 20
         t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=32 << 30)
@@ -678,7 +681,8 @@ def run_other(args):
             if s >= args.warmup:
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(5 * n)
-        launches = 3 + 2 + 2
+        # 3 finds; assign: clear, dedup, assign; upsert: clear, stage, bucket
+        launches = 3 + 3 + 3
     torch.cuda.nvtx.range_pop()
     counts = t.op_counts()
     total = sum(times)
