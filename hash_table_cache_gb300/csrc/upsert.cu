@@ -970,7 +970,13 @@ __device__ __forceinline__ void stage_routed(const TableView& t, const UpsertScr
 // Pass 1: resident keys update value (and score) in place; absent keys are
 // flagged in the dedup map (for the counts) and routed.  One 8-lane tile per
 // key.
-__global__ void __launch_bounds__(kThreads, 4) dual_route_kernel(
+#ifndef HKV_ASSIGN_MIN_BLOCKS
+#define HKV_ASSIGN_MIN_BLOCKS 6
+#endif
+#ifndef HKV_ROUTE_MIN_BLOCKS
+#define HKV_ROUTE_MIN_BLOCKS 8
+#endif
+__global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
     ScoreRule rule, bool vec) {
   pdl_wait();
@@ -1081,7 +1087,7 @@ __global__ void dual_finish_kernel(TableView t, UpsertScratch sc) {
 // ---------------------------------------------------------------------------
 // assign (updater) and erase (inserter).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) assign_kernel(TableView t, UpsertScratch sc, uint64_t n,
+__global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel(TableView t, UpsertScratch sc, uint64_t n,
                                                           const uint64_t* keys, const float* values,
                                                           ScoreRule rule, bool keep_scores,
                                                           bool vec) {
