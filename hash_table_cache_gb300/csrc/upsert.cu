@@ -263,6 +263,11 @@ struct alignas(16) BucketStage {
   alignas(16) uint32_t dhead[256];  // digest -> first slot carrying it (0xFF: none)
   uint8_t dnext[kSlots];            // next slot with the same digest (0xFF: end)
   uint8_t list[kSlots];             // free-slot list, later the dirty-slot list
+  // insert_and_evict: the value rows of one extraction round to report
+  // (output index, source batch index or kNone, slot), at most 32
+  uint32_t ev_o[32];
+  uint32_t ev_src[32];
+  uint8_t ev_slot[32];
   alignas(16) uint64_t einc[kLfu ? kWin * 32 : 2];  // summed increments (LFU policies)
 #if HKV_UPSERT_PIPELINE
   // The warp's next bucket, brought in by the copy engine while this one is
@@ -400,7 +405,7 @@ __device__ __noinline__ ExactOut extract_exact(const Stage* st, unsigned lane, u
 constexpr int kCopyWaitLimit = 1 << 14;
 #endif
 
-template <bool kLfu, bool kDual>
+template <bool kLfu, bool kDual, bool kEvict>
 __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_single_kernel(
     TableView t, UpsertScratch scr, const uint64_t* keys_in, const float* values_in,
     ScoreRule rule, bool vec, UpsertExtra ex) {
@@ -693,30 +698,45 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
       // Extracted bucket entries: list them in slot order for the pending keys.
       uint32_t n_ext;
       uint32_t pos = prefix_small(static_cast<uint32_t>(__popc(rem)), n_ext);
-      uint32_t ev = 0, fr = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (rem & (1u << q)) {
+      for (int q = 0; q < 4; ++q)
+        if (rem & (1u << q)) st.list[pos++] = static_cast<uint8_t>(lane * 4 + q);
+      // extracted entries placed earlier this call (fresh) vs pre-call residents
+      const uint32_t evm = rem & ~fw & 15u;
+      const uint32_t ev = __popc(evm), fr = __popc(rem & fw & 15u);
+      if (kEvict && ex.ev_keys) {
+        // insert_and_evict: report the displaced pre-call residents as they
+        // are now, at output positions taken with one atomic per warp
+        uint32_t n_out;
+        uint32_t at = prefix_small(ev, n_out);
+        unsigned long long o0 = 0;
+        if (lane == 0 && n_out) o0 = atomicAdd(ex.ev_count, static_cast<unsigned long long>(n_out));
+        o0 = __shfl_sync(0xFFFFFFFFu, o0, 0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (!((evm >> q) & 1u)) continue;
           const uint32_t slot = lane * 4 + q;
-          st.list[pos++] = static_cast<uint8_t>(slot);
-          if ((fw >> q) & 1u) {
-            ++fr;  // admitted earlier this call
-          } else {
-            ++ev;  // pre-call resident
-            if (ex.ev_keys) {  // insert_and_evict: report it as it is now
-              const unsigned long long o = atomicAdd(ex.ev_count, 1ull);
-              ex.ev_keys[o] = st.key[slot];
-              if (ex.ev_scores) ex.ev_scores[o] = st.score[slot];
-              if (ex.ev_values) {
-                const uint32_t src_i = st.occ[slot];  // updated by this call: its input row
-                const float* src = src_i != kNone ? values_in + static_cast<uint64_t>(src_i) * t.dim
-                                                  : row_ptr(t, b * kSlots + slot);
-                float* dst = ex.ev_values + o * t.dim;
-                for (uint32_t c = 0; c < t.dim; ++c) dst[c] = src[c];
-              }
-            }
+          const unsigned long long o = o0 + at;
+          ex.ev_keys[o] = st.key[slot];
+          if (ex.ev_scores) ex.ev_scores[o] = st.score[slot];
+          st.ev_o[at] = static_cast<uint32_t>(o);
+          st.ev_src[at] = st.occ[slot];  // updated by this call: its input row
+          st.ev_slot[at] = static_cast<uint8_t>(slot);
+          ++at;
+        }
+        __syncwarp();
+        if (ex.ev_values) {  // the rows, 8-lane tiles, 16-byte vectors when aligned
+          const bool evec = vec && (reinterpret_cast<uintptr_t>(ex.ev_values) & 15) == 0;
+          for (uint32_t j = lane >> 3; j < n_out; j += 4) {
+            const uint32_t src_i = st.ev_src[j];
+            const float* src = src_i != kNone
+                                   ? values_in + static_cast<uint64_t>(src_i) * t.dim
+                                   : row_ptr(t, b * kSlots + st.ev_slot[j]);
+            tile_copy_row(ex.ev_values + static_cast<uint64_t>(st.ev_o[j]) * t.dim, src, t.dim,
+                          sub, evec, true);
           }
         }
+        __syncwarp();
       }
       if (kDual && ex.collect_retry) {
         // keys of the batch this pass displaced (rejected absent keys and
@@ -1273,8 +1293,26 @@ __global__ void __launch_bounds__(kThreads) clear_scratch_kernel(UpsertScratch s
     for (uint64_t i = tid; i < mark_bytes; i += stride) s.mark[i] = 0;
 }
 
+template <bool kLfu, bool kDual, bool kEvict>
+cudaError_t launch_bucket_kernel(unsigned grid, const TableView& t, const UpsertScratch& s,
+                                 const uint64_t* keys, const float* values, const ScoreRule& r,
+                                 bool vec, cudaStream_t st, const UpsertExtra& ex) {
+  const size_t smem =
+      HKV_UPSERT_PIPELINE ? sizeof(BucketStage<kLfu>) * (kBucketThreads / 32) : 0;
+  if (smem) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(upsert_single_kernel<kLfu, kDual, kEvict>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_chained(upsert_single_kernel<kLfu, kDual, kEvict>, grid, kBucketThreads, smem, st,
+                        t, s, keys, values, r, vec, ex);
+}
+
 // One bucket pass (single or dual mode).  Non-LFU rules become one score per
 // call (the clock, folded with the epoch) unless the caller gives scores.
+// insert_and_evict (single mode only) runs its own instance of the kernel,
+// so the plain upsert carries none of the reporting code.
 template <bool kDual>
 cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
                                const float* values, const ScoreRule& rule, bool vec,
@@ -1283,27 +1321,20 @@ cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const
   uint64_t blocks = (t.num_buckets * 32 + kBucketThreads - 1) / kBucketThreads;
   const uint64_t cap = static_cast<uint64_t>(sm_count()) * HKV_UPSERT_MIN_BLOCKS;
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  cudaError_t e = cudaSuccess;
-  if (rule.lfu()) {
-    const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<true>) * (kBucketThreads / 32) : 0;
-    if (smem)
-      e = cudaFuncSetAttribute(upsert_single_kernel<true, kDual>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return launch_chained(upsert_single_kernel<true, kDual>, grid, kBucketThreads, smem, st, t, s, keys,
-                          values, rule, vec, ex);
-  }
+  const bool evict = !kDual && ex.ev_keys != nullptr;
+  if (rule.lfu())
+    return evict ? launch_bucket_kernel<true, kDual, !kDual>(grid, t, s, keys, values, rule, vec,
+                                                             st, ex)
+                 : launch_bucket_kernel<true, kDual, false>(grid, t, s, keys, values, rule, vec,
+                                                            st, ex);
   ScoreRule r = rule;
   if (rule.policy != kCustomized) r.in = nullptr;
   if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
   r.policy = kCustomized;
-  const size_t smem = HKV_UPSERT_PIPELINE ? sizeof(BucketStage<false>) * (kBucketThreads / 32) : 0;
-  if (smem)
-    e = cudaFuncSetAttribute(upsert_single_kernel<false, kDual>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return launch_chained(upsert_single_kernel<false, kDual>, grid, kBucketThreads, smem, st, t, s, keys,
-                        values, r, vec, ex);
+  return evict ? launch_bucket_kernel<false, kDual, !kDual>(grid, t, s, keys, values, r, vec, st,
+                                                            ex)
+               : launch_bucket_kernel<false, kDual, false>(grid, t, s, keys, values, r, vec, st,
+                                                           ex);
 }
 
 }  // namespace
