@@ -114,9 +114,9 @@ def upsert_access_floor(n, dim, rows_written, buckets_touched, rates, hbm_gbs):
 NCU_TRAFFIC = {
     "find_kernel": {"bytes": 164755712 + 69267968, "sources": ("find.cu", "common.cuh", "launch.h"),
                     "sha256": "2f71ef7c08587846"},
-    "upsert_single_kernel": {"bytes": 180340736 + 60790016,
+    "upsert_single_kernel": {"bytes": 180330496 + 61313536,
                              "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "2420e2e798aebd03"},
+                             "sha256": "9e6740b699809826"},
 }
 
 
