@@ -151,7 +151,9 @@ class Clocks:
         self.dev = device_index
         self.proc = None
         self.window = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(),
+                                 f"hkv_bench_clocks_{os.getpid()}_{device_index}.csv")
 
     def __enter__(self):
         try:
