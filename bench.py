@@ -210,6 +210,28 @@ class Clocks:
                 "reasons": reasons, "samples": len(sel)}
 
 
+def replica_seed_base(rank):
+    """Replicas (one per rank) draw disjoint key streams: every seed of rank r
+    is offset by 1000 r."""
+    return 1000 * rank
+
+
+def job_time_and_value(total_s, keys_this_rank, world, device=None):
+    """Whole-job figures of the replicas: the slowest rank's timed total
+    (max over ranks) and keys of all ranks / that time in B-KV/s.  The only
+    collectives of the run (the data path has none)."""
+    keys_all = float(keys_this_rank)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_s], dtype=torch.float64, device=device)
+        k = torch.tensor([keys_all], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(k, op=dist.ReduceOp.SUM)
+        total_s, keys_all = float(t.item()), float(k.item())
+    return total_s, keys_all / total_s / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -232,7 +254,7 @@ def run_gpu(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     hkv.load()
-    seed_base = 1000 * rank
+    seed_base = replica_seed_base(rank)
 
     def dk(a):
         return torch.from_numpy(wl.as_i64(a)).to(dev)
@@ -346,12 +368,7 @@ def run_gpu(args):
     fi_t = [ev[s][1].elapsed_time(ev[s][2]) * 1e-3 for s in range(args.warmup, nsteps)]
     total = sum(up_t) + sum(fi_t)
     counts = t.op_counts()
-    if world > 1:
-        tt = torch.tensor([total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total = float(tt.item())
-    keys_done = 2 * BATCH * args.steps * world
-    value = keys_done / total / 1e9
+    total, value = job_time_and_value(total, 2 * BATCH * args.steps, world, dev)
 
     # roofline: find is one kernel per call, timed exactly by the events
     # around hkv_find; insert_or_assign is a call of two kernels (stage +
