@@ -663,9 +663,9 @@ def run_other(args):
             if s >= args.warmup:
                 times.append(a.elapsed_time(b) * 1e-3)
                 nkeys.append(2 * n)
-        # clear, dedup, route, bucket pass, clear, retry, bucket pass, count,
-        # finish, find
-        launches = 10
+        # clear, dedup, route, bucket pass, clear, retry, bucket pass, finish,
+        # find
+        launches = 9
     elif cfg == "c5":
         cap, dim, n = 1 << 28, 64, 1 << 20
         t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=32 << 30)

@@ -163,6 +163,10 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
+// Hint: bring the 128-byte line holding p (global memory) into L2; no result.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // Streaming read: no L1 allocation (value rows are touched once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 r;

@@ -47,6 +47,10 @@ constexpr int kBucketThreads = HKV_BUCKET_THREADS;  // bucket kernel block size
 #ifndef HKV_UPSERT_PIPELINE
 #define HKV_UPSERT_PIPELINE 0
 #endif
+// L2 prefetch of the warp's next bucket and of the entries' input rows
+#ifndef HKV_UPSERT_PREFETCH
+#define HKV_UPSERT_PREFETCH 1
+#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 
 __device__ __forceinline__ uint32_t map_home(uint64_t key, uint32_t mask) {
@@ -64,8 +68,31 @@ __device__ __forceinline__ uint32_t map_find(const uint64_t* mkeys, uint32_t mas
   return kNone;
 }
 
+// Whether `key` is a key of the running dual-mode call that was absent when
+// the call began (its dedup-map entry carries pass 1's absent flag).
+__device__ __forceinline__ bool absent_in_call(const UpsertScratch& sc, uint64_t key) {
+  const uint32_t s = map_find(sc.map_keys, sc.map_size - 1, key);
+  return s != kNone && sc.map_keys[s] == key && sc.absent[s];
+}
+
 // Map entry of `key` when batch index i is its last occurrence, else kNone,
-// looked up by the 8 lanes of a tile: they read 8 consecutive probe
+// looked up by one thread (the dual-mode kernels keep a warp's 32 lookups in
+// flight together).  Each probe position's key and index are read together.
+__device__ __forceinline__ uint32_t map_last_occurrence(const UpsertScratch& sc, uint64_t key,
+                                                        uint64_t i) {
+  const uint32_t mask = sc.map_size - 1;
+  uint32_t s = map_home(key, mask);
+  for (uint32_t p = 0; p <= mask; ++p) {
+    const uint64_t v = sc.map_keys[s];
+    const uint32_t idx = sc.map_idx[s];
+    if (v == key) return idx == static_cast<uint32_t>(i) + 1 ? s : kNone;
+    if (v == kEmptyKey) return kNone;
+    s = (s + 1) & mask;
+  }
+  return kNone;
+}
+
+// The same lookup by the 8 lanes of a tile: they read 8 consecutive probe
 // positions at once, one round trip per 8 positions.
 __device__ __forceinline__ uint32_t tile_last_occurrence(const UpsertScratch& sc, uint64_t key,
                                                          uint64_t i, unsigned sub,
@@ -461,9 +488,33 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
   for (; b < nb; b = b_next) {
     b_next = owned_from(b + nwarps);
 #else
-  for (uint64_t b = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nb;
-       b += nwarps) {
-    if (scr.mark && !scr.mark[b]) continue;  // no key of the batch here
+  // The warp's buckets b0, b0 + W, b0 + 2W, ... (W warps in the grid) that
+  // hold a key of the batch (all of them without a mark array), 32 at a
+  // time: one mark load per lane, then the set bits of the ballot in order.
+  uint64_t g = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  auto marked = [&](uint64_t g0) -> unsigned {
+    const uint64_t x = g0 + lane * nwarps;
+    return __ballot_sync(0xFFFFFFFFu, x < nb && (!scr.mark || scr.mark[x]));
+  };
+  unsigned todo = marked(g);
+  auto next_bucket = [&]() -> uint64_t {
+    while (!todo) {
+      g += 32 * nwarps;
+      if (g >= nb) return nb;
+      todo = marked(g);
+    }
+    const uint64_t x = g + (__ffs(todo) - 1) * nwarps;
+    todo &= todo - 1;
+    return x;
+  };
+  for (uint64_t b = next_bucket(); b < nb; b = next_bucket()) {
+#if HKV_UPSERT_PREFETCH
+    if (todo) {  // the warp's next bucket: its pairs and digest line into L2
+      const uint64_t bn = g + (__ffs(todo) - 1) * nwarps;
+      if (lane < 16) prefetch_l2(key_at(t, bn * kSlots + lane * 8));
+      else if (lane == 16) prefetch_l2(t.digests + bn * kSlots);
+    }
+#endif
 #endif
     const uint64_t base = b * kSlots + lane * 4;
     // This bucket's stage run: from lo, past a_end, up to the first free
@@ -565,6 +616,15 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
     for (int w = 0; w < kWin; ++w)
       we[w] = w < static_cast<int>(nw) ? entry_of(w, wk[w], wr[w], wb[w]) : kNone;
     const bool in_window = run_ended;  // the run ends inside the loaded chunks
+#if HKV_UPSERT_PREFETCH
+    // the entries' input value rows (phase C copies them) into L2
+#pragma unroll
+    for (int w = 0; w < kWin; ++w) {
+      if (we[w] == kNone) continue;
+      const char* row = reinterpret_cast<const char*>(values_in + static_cast<uint64_t>(we[w]) * t.dim);
+      for (uint32_t off = 0; off < 4 * t.dim; off += 128) prefetch_l2(row + off);
+    }
+#endif
     __syncwarp();
 
     // Phase A (Algorithm 2, found branch): a resident key gets its new value
@@ -756,8 +816,16 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
           if ((rem >> q) & (fw >> q) & 1u) scr.retry[base_r++] = st.occ[lane * 4 + q];
         if (rej) scr.retry[base_r] = e;
       }
+      uint32_t fr_all = fr;
+      if (kDual && !ex.collect_retry) {
+        // second pass: an extracted entry that the first pass placed is a key
+        // of this call that ends up absent, not an eviction
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (((evm >> q) & 1u) && absent_in_call(scr, st.key[lane * 4 + q])) ++fr_all;
+      }
       const uint32_t n_ev = __reduce_add_sync(0xFFFFFFFFu, ev);
-      const uint32_t n_fr = __reduce_add_sync(0xFFFFFFFFu, fr);
+      const uint32_t n_fr = __reduce_add_sync(0xFFFFFFFFu, fr_all);
       if (lane == 0) {
         n_evi += n_ev;
         n_adm -= n_fr;
@@ -916,8 +984,10 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
   if (in_flight) wait_copy(parity);  // only after a timed-out wait: let the copy land first
 #endif
   if (lane == 0) {
-    if (kDual) {  // dual_count_kernel / dual_finish_kernel produce the counts
+    if (kDual) {  // dual_finish_kernel turns these into the call's counts
       if (n_fill) atomicAdd(&t.stats->fills, n_fill);
+      // net admitted keys of this pass (two's complement: may be negative)
+      if (n_adm) atomicAdd(reinterpret_cast<unsigned long long*>(scr.cursor + 2), n_adm);
     } else {
       if (n_upd) atomicAdd(&t.stats->updated, n_upd);
       if (n_adm) atomicAdd(&t.stats->admitted, n_adm);
@@ -987,14 +1057,149 @@ __device__ __forceinline__ void stage_routed(const TableView& t, const UpsertScr
   sc.mark[target] = 1;
 }
 
+// Probe both candidate buckets of U dual-mode keys with the 8 lanes of a tile
+// (HKV §3.4: two fixed-length line loads per key): the 2U digest lines are
+// loaded together, then every key's first digest match is confirmed, those
+// key loads in flight together too.  slot[u] is the slot or -1, bkt[u] the
+// bucket holding the key; uniform across the tile.  Read-only loads: no
+// thread of the calling kernels writes keys or digests.
+template <int U>
+__device__ __forceinline__ void tile_probe_pair_many(const TableView& t, const uint64_t (&b1)[U],
+                                                     const uint64_t (&b2)[U],
+                                                     const uint64_t (&k)[U],
+                                                     const uint32_t (&pat)[U],
+                                                     const bool (&act)[U], unsigned sub,
+                                                     unsigned tmask, int (&slot)[U],
+                                                     uint64_t (&bkt)[U]) {
+  uint4 g1[U], g2[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (act[u]) {
+      g1[u] = ld_nc_v4(t.digests + b1[u] * kSlots + sub * 16);
+      g2[u] = ld_nc_v4(t.digests + b2[u] * kSlots + sub * 16);
+    }
+  }
+  // bits 0-15: the lane's 16 bytes of b1's line; bits 16-31: of b2's
+  uint32_t m[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    m[u] = 0;
+    if (act[u])
+      m[u] = byte_match4(g1[u].x, pat[u]) | (byte_match4(g1[u].y, pat[u]) << 4) |
+             (byte_match4(g1[u].z, pat[u]) << 8) | (byte_match4(g1[u].w, pat[u]) << 12) |
+             (byte_match4(g2[u].x, pat[u]) << 16) | (byte_match4(g2[u].y, pat[u]) << 20) |
+             (byte_match4(g2[u].z, pat[u]) << 24) | (byte_match4(g2[u].w, pat[u]) << 28);
+  }
+  auto key_ptr = [&](int u, int bit) {
+    const uint64_t b = bit < 16 ? b1[u] : b2[u];
+    return key_at(t, b * kSlots + sub * 16 + static_cast<uint32_t>(bit & 15));
+  };
+  uint64_t first[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (m[u]) first[u] = ld_nc_u64(key_ptr(u, __ffs(m[u]) - 1));
+  int hit[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    hit[u] = -1;
+    if (!m[u]) continue;
+    int bit = __ffs(m[u]) - 1;
+    if (first[u] == k[u]) {
+      hit[u] = bit;
+      continue;
+    }
+    m[u] &= m[u] - 1;
+    while (m[u]) {  // further digest matches (rare)
+      bit = __ffs(m[u]) - 1;
+      m[u] &= m[u] - 1;
+      if (ld_nc_u64(key_ptr(u, bit)) == k[u]) {
+        hit[u] = bit;
+        break;
+      }
+    }
+  }
+  // a key sits in at most one of its buckets: code = slot, +128 for b2
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
+    int code = hit[u] < 0 ? -1
+                          : static_cast<int>(sub * 16) + (hit[u] & 15) + ((hit[u] & 16) ? 128 : 0);
+    code = bal ? __shfl_sync(tmask, code, __ffs(bal) - 1) : -1;
+    slot[u] = code < 0 ? -1 : (code & 127);
+    bkt[u] = code >= 128 ? b2[u] : b1[u];
+  }
+}
+
+// Dual-mode pass 1 takes 32 consecutive keys per warp: the dedup lookup and
+// the per-key follow-up run one key per lane, so a warp keeps 32 keys'
+// accesses in flight; the two-line bucket probe runs on the warp's four
+// 8-lane tiles, each probing the keys of its own 8 lanes, kRouteKeysPerTile
+// at a time, and copying the input rows of the resident ones over their
+// table rows.  Result: the lane's own key's slot (or -1) and bucket.  `live`
+// selects the lanes whose key is probed.
+#ifndef HKV_ROUTE_KEYS_PER_TILE
+#define HKV_ROUTE_KEYS_PER_TILE 2
+#endif
+constexpr int kRouteKeysPerTile = HKV_ROUTE_KEYS_PER_TILE;
+
+__device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k, uint64_t h,
+                                                uint64_t b1, uint64_t b2, bool live,
+                                                const float* values, uint64_t base, bool vec,
+                                                uint64_t& bkt) {
+  constexpr int U = kRouteKeysPerTile;
+  const unsigned lane = lane_id();
+  const unsigned sub = lane & 7u;
+  const unsigned tile0 = lane & 24u;
+  const unsigned tmask = 0xFFu << tile0;
+  const uint32_t my_pat = digest_of_hash(h) * 0x01010101u;
+  int my_slot = -1;
+  bkt = b1;
+#pragma unroll 1
+  for (int r = 0; r < 8; r += U) {
+    uint64_t kk[U], c1[U], c2[U];
+    uint32_t pat[U];
+    bool act[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int src = static_cast<int>(tile0) + r + u;
+      kk[u] = __shfl_sync(0xFFFFFFFFu, k, src);
+      c1[u] = __shfl_sync(0xFFFFFFFFu, b1, src);
+      c2[u] = __shfl_sync(0xFFFFFFFFu, b2, src);
+      pat[u] = __shfl_sync(0xFFFFFFFFu, my_pat, src);
+      act[u] = __shfl_sync(0xFFFFFFFFu, live ? 1 : 0, src) != 0;
+    }
+    int slot[U];
+    uint64_t bk[U];
+    tile_probe_pair_many<U>(t, c1, c2, kk, pat, act, sub, tmask, slot, bk);
+    // resident keys: U row copies in flight
+    float* dst[U];
+    const float* src[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ok[u] = slot[u] >= 0;
+      dst[u] = ok[u] ? row_ptr(t, bk[u] * kSlots + static_cast<uint64_t>(slot[u])) : nullptr;
+      src[u] = ok[u] ? values + (base + tile0 + r + u) * t.dim : values;
+    }
+    tile_copy_rows<U>(dst, src, ok, t.dim, sub, vec);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (sub == static_cast<unsigned>(r + u)) {
+        my_slot = slot[u];
+        bkt = bk[u];
+      }
+    }
+  }
+  return my_slot;
+}
+
 // Pass 1: resident keys update value (and score) in place; absent keys are
-// flagged in the dedup map (for the counts) and routed.  One 8-lane tile per
-// key.
+// flagged in the dedup map (for the counts) and routed.
 #ifndef HKV_ASSIGN_MIN_BLOCKS
 #define HKV_ASSIGN_MIN_BLOCKS 6
 #endif
 #ifndef HKV_ROUTE_MIN_BLOCKS
-#define HKV_ROUTE_MIN_BLOCKS 8
+#define HKV_ROUTE_MIN_BLOCKS 4
 #endif
 __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
@@ -1002,39 +1207,36 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
   pdl_wait();
   pdl_trigger();
   const unsigned lane = lane_id();
-  const unsigned sub = lane & 7u;
-  const unsigned tmask = 0xFFu << (lane & 24u);
-  const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
-  unsigned long long upd = 0;
-  for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
-       i += tiles) {
-    const uint64_t k = keys[i];
-    if (is_reserved(k)) continue;
-    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
-    if (ms == kNone) continue;
+  const uint64_t warps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
+  unsigned long long upd = 0, absent = 0;
+  for (uint64_t base = ((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 32;
+       base < n; base += warps * 32) {
+    const uint64_t i = base + lane;
+    const uint64_t k = i < n ? keys[i] : kEmptyKey;
+    const uint32_t ms = i < n && !is_reserved(k) ? map_last_occurrence(sc, k, i) : kNone;
+    const bool live = ms != kNone;  // the key's last occurrence in the batch
     const uint64_t h = hash64(k);
-    const uint32_t pat = digest_of_hash(h) * 0x01010101u;
     const uint64_t b1 = bucket_of_hash(t, h);
     const uint64_t b2 = bucket2_of(t, k, b1);
-    uint64_t b = b1;
-    int slot = tile_probe_pair<true>(t, b1, b2, k, pat, sub, tmask, b);
+    uint64_t b;
+    const int slot = warp_probe_update(t, k, h, b1, b2, live, values, base, vec, b);
+    if (!live) continue;
+    sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
+    const uint64_t inc = entry_inc(sc, ms);
     if (slot >= 0) {
-      const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
-      tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
-      if (sub == 0) {
-        uint64_t* sp = score_at(t, row);
-        *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
-        ++upd;
-      }
-    }
-    if (sub == 0) sc.absent[ms] = slot < 0 ? 1 : 0;  // for dual_count_kernel
-    if (slot < 0 && sub == 0) {
-      const uint64_t inc = entry_inc(sc, ms);
+      uint64_t* sp = score_at(t, b * kSlots + static_cast<uint64_t>(slot));
+      *sp = policy_score(rule, i, inc, true, rule.lfu() ? *sp : 0ull);
+      ++upd;
+    } else {
+      ++absent;
       const uint64_t target = route_bucket(t, b1, b2, policy_score(rule, i, inc, false, 0));
       if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
     }
   }
   warp_add(&t.stats->updated, upd);
+  // the call's absent keys; dual_finish_kernel splits them into admitted
+  // and rejected
+  warp_add(reinterpret_cast<unsigned long long*>(sc.cursor + 6), absent);
 }
 
 // Pass 2: the keys the first bucket pass displaced are routed again with the
@@ -1059,46 +1261,16 @@ __global__ void __launch_bounds__(kThreads) dual_retry_kernel(TableView t, Upser
   }
 }
 
-// After placement: count admitted (resident) vs rejected absent keys.
-__global__ void __launch_bounds__(kThreads) dual_count_kernel(TableView t, UpsertScratch sc,
-                                                              uint64_t n, const uint64_t* keys) {
-  const unsigned lane = lane_id();
-  const unsigned sub = lane & 7u;
-  const unsigned tmask = 0xFFu << (lane & 24u);
-  const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
-  unsigned long long adm = 0, rej = 0;
-  for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
-       i += tiles) {
-    const uint64_t k = keys[i];
-    if (is_reserved(k)) continue;
-    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
-    if (ms == kNone || !sc.absent[ms]) continue;  // a duplicate, or resident before the call
-    const uint64_t h = hash64(k);
-    const uint32_t pat = digest_of_hash(h) * 0x01010101u;
-    const uint64_t b1 = bucket_of_hash(t, h);
-    uint64_t b;
-    const int slot = tile_probe_pair<true>(t, b1, bucket2_of(t, k, b1), k, pat, sub, tmask, b);
-    if (sub == 0) {
-      if (slot >= 0) ++adm;
-      else ++rej;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    adm += __shfl_xor_sync(0xFFFFFFFFu, adm, o);
-    rej += __shfl_xor_sync(0xFFFFFFFFu, rej, o);
-  }
-  if (lane == 0) {
-    if (adm) atomicAdd(&t.stats->admitted, adm);
-    if (rej) atomicAdd(&t.stats->rejected, rej);
-    // this call's admitted count; dual_finish_kernel turns it into evictions
-    if (adm) atomicAdd(reinterpret_cast<unsigned long long*>(sc.cursor + 2), adm);
-  }
-}
-
-// evicted = admitted - fills for the call; size grows by fills.
+// The call's counts: admitted = the bucket passes' net placements (keys of
+// the call resident at its end), rejected = absent keys - admitted, evicted =
+// admitted - fills (every other admitted key displaced a resident); size
+// grows by fills.
 __global__ void dual_finish_kernel(TableView t, UpsertScratch sc) {
   const unsigned long long adm = *reinterpret_cast<unsigned long long*>(sc.cursor + 2);
+  const unsigned long long absent = *reinterpret_cast<unsigned long long*>(sc.cursor + 6);
   const unsigned long long fills = t.stats->fills;
+  t.stats->admitted += adm;
+  t.stats->rejected += absent - adm;
   t.stats->evicted += adm - fills;
   t.stats->size += fills;
   t.stats->fills = 0;
@@ -1366,8 +1538,8 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   // them bucket by bucket; route the displaced ones once more and place
   // them; count.
   dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, inc_in, t.stats);
-  e = launch_chained(dual_route_kernel, grid_for(n * 8), kThreads, 0, st, t, s, n, keys, values,
-                     rule, vec);
+  e = launch_chained(dual_route_kernel, grid_for(n, HKV_ROUTE_MIN_BLOCKS), kThreads, 0, st, t, s,
+                     n, keys, values, rule, vec);
   UpsertExtra first = ex;
   first.collect_retry = true;
   if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, first);
@@ -1378,7 +1550,6 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
     e = launch_chained(dual_retry_kernel, grid_for(n), kThreads, 0, st, t, s, keys, rule);
   if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, ex);
   if (e != cudaSuccess) return e;
-  dual_count_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys);
   dual_finish_kernel<<<1, 1, 0, st>>>(t, s);
   return cudaGetLastError();
 }

@@ -99,6 +99,8 @@ def test_dual_bucket_invariants(hkv, oracle_mod):
         c = t.op_counts()
         assert c["admitted"] + c["rejected"] == k.size and c["updated"] == 0
         assert t.size() == before + c["admitted"] - c["evicted"]
+        # every key of the batch was absent: admitted = those resident now
+        assert c["admitted"] == int(t.contains(dkeys(k)).sum().item())
         if i % 4 == 3:
             _check_dual_invariants(t, o, last_score, last_salt, dim)
     assert t.error_counts()["timeouts"] == 0
@@ -133,6 +135,51 @@ def test_dual_bucket_invariants(hkv, oracle_mod):
     ora_ret = len(top & set(o.export()[0].tolist())) / n_top
     print(f"dual top-N retention: gpu {gpu_ret:.4f} oracle {ora_ret:.4f}")
     assert gpu_ret > 0.95 and abs(gpu_ret - ora_ret) < 0.02
+
+
+@pytest.mark.parametrize("policy", ["custom", "lru"])
+def test_dual_counts_mixed_batches(hkv, oracle_mod, policy):
+    """Dual mode on a full table with batches that mix resident keys, fresh
+    keys and repeats (fresh keys with tied step scores under LRU): the
+    per-call counts agree with the table afterwards -- updated = distinct
+    resident keys, admitted = distinct fresh keys now resident, admitted +
+    rejected = distinct fresh keys, size grows by admitted - evicted -- and
+    the invariants hold."""
+    B, dim, bs = 384, 4, 6000
+    cap = B * 128
+    mode = hkv.HKV_MODE_DUAL | (0 if policy == "custom" else hkv.HKV_POLICY_LRU)
+    t = hkv.HashTable(cap, dim, mode=mode)
+    keys = wl.unique_keys(91, 3 * cap)
+    scores = wl.stream(92, keys.size) >> np.uint64(2)
+    custom = policy == "custom"
+    pos = 0
+    while t.size() < cap and pos < cap * 2:
+        k = keys[pos:pos + bs]
+        t.insert_or_assign(dkeys(k), dvals(wl.key_values(k, dim, salt=1)),
+                           dkeys(scores[pos:pos + bs]) if custom else None)
+        pos += bs
+    rng = np.random.default_rng(93)
+    for r in range(6):
+        res = u64(t.export(with_values=False)[0])
+        fresh = keys[pos:pos + int(0.6 * bs)]
+        pos += fresh.size
+        old = rng.choice(res, int(0.3 * bs), replace=False)
+        batch = np.concatenate([fresh, old])
+        batch = np.concatenate([batch, rng.choice(batch, bs - batch.size)])  # repeats
+        rng.shuffle(batch)
+        sc = wl.stream(94 + r, batch.size) >> np.uint64(2)
+        t.reset_op_counts()
+        before = t.size()
+        t.insert_or_assign(dkeys(batch), dvals(wl.key_values(batch, dim, salt=10 + r)),
+                           dkeys(sc) if custom else None)
+        c = t.op_counts()
+        fresh_u = np.unique(fresh)
+        assert c["updated"] == np.unique(old).size
+        assert c["admitted"] + c["rejected"] == fresh_u.size
+        assert c["admitted"] == int(t.contains(dkeys(fresh_u)).sum().item())
+        assert t.size() == before + c["admitted"] - c["evicted"]
+        assert c["evicted"] <= c["admitted"]
+    assert t.error_counts()["timeouts"] == 0
 
 
 def test_tiered_equals_hbm_only(hkv, oracle_mod):
