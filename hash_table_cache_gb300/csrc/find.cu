@@ -28,71 +28,6 @@ namespace {
 
 constexpr int kFindKeysPerTile = HKV_FIND_KEYS_PER_TILE;
 
-// Probe for U keys at once: the U digest-line loads, then the U first-match
-// (key, score) pair loads, are issued back to back so a tile keeps U requests
-// in flight.  Returns the slot (or -1) and, on a hit, the score, which comes
-// with the key in the same 16-byte load.
-template <int U>
-__device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64_t (&b)[U],
-                                                const uint64_t (&k)[U], const uint32_t (&pat)[U],
-                                                const bool (&act)[U], unsigned sub, unsigned tmask,
-                                                int (&slot)[U],
-                                                uint64_t (&score)[U]) {
-  uint4 dg[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-    if (act[u]) dg[u] = ld_nc_v4(t.digests + b[u] * kSlots + sub * 16);
-  uint32_t m[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    m[u] = 0;
-    if (act[u])
-      m[u] = byte_match4(dg[u].x, pat[u]) | (byte_match4(dg[u].y, pat[u]) << 4) |
-             (byte_match4(dg[u].z, pat[u]) << 8) | (byte_match4(dg[u].w, pat[u]) << 12);
-  }
-  ulonglong2 kk[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (m[u]) {
-      const uint64_t row = b[u] * kSlots + sub * 16 + (__ffs(m[u]) - 1);
-      kk[u] = ld_nc_pair(key_at(t, row));
-    }
-  }
-  int hit[U];
-  uint64_t hs[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    hit[u] = -1;
-    hs[u] = 0;
-    if (m[u]) {
-      int bit = __ffs(m[u]) - 1;
-      if (kk[u].x == k[u]) {
-        hit[u] = static_cast<int>(sub * 16 + bit);
-        hs[u] = kk[u].y;
-      } else {
-        m[u] &= m[u] - 1;
-        while (m[u]) {  // further digest matches (rare)
-          bit = __ffs(m[u]) - 1;
-          m[u] &= m[u] - 1;
-          const ulonglong2 p = ld_nc_pair(key_at(t, b[u] * kSlots + sub * 16 + bit));
-          if (p.x == k[u]) {
-            hit[u] = static_cast<int>(sub * 16 + bit);
-            hs[u] = p.y;
-            break;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
-    const int lead = bal ? __ffs(bal) - 1 : static_cast<int>(lane_id());
-    slot[u] = bal ? __shfl_sync(tmask, hit[u], lead) : -1;
-    score[u] = __shfl_sync(tmask, hs[u], lead);
-  }
-}
-
 // Digest ablation (HKV §5.4, Table 7): the same probe without the digest
 // line.  The tile compares the key against every slot's key: lane `sub`
 // reads the (key, score) pairs of slots sub, sub+8, ..., 16 bytes per lane

@@ -76,8 +76,8 @@ __device__ __forceinline__ bool absent_in_call(const UpsertScratch& sc, uint64_t
 }
 
 // Map entry of `key` when batch index i is its last occurrence, else kNone,
-// looked up by one thread (the dual-mode kernels keep a warp's 32 lookups in
-// flight together).  Each probe position's key and index are read together.
+// looked up by one thread (the warp-per-32-keys kernels keep a warp's 32
+// lookups in flight together).  Each probe position's key and index are read together.
 __device__ __forceinline__ uint32_t map_last_occurrence(const UpsertScratch& sc, uint64_t key,
                                                         uint64_t i) {
   const uint32_t mask = sc.map_size - 1;
@@ -88,28 +88,6 @@ __device__ __forceinline__ uint32_t map_last_occurrence(const UpsertScratch& sc,
     if (v == key) return idx == static_cast<uint32_t>(i) + 1 ? s : kNone;
     if (v == kEmptyKey) return kNone;
     s = (s + 1) & mask;
-  }
-  return kNone;
-}
-
-// The same lookup by the 8 lanes of a tile: they read 8 consecutive probe
-// positions at once, one round trip per 8 positions.
-__device__ __forceinline__ uint32_t tile_last_occurrence(const UpsertScratch& sc, uint64_t key,
-                                                         uint64_t i, unsigned sub,
-                                                         unsigned tmask) {
-  const uint32_t mask = sc.map_size - 1;
-  const uint32_t home = map_home(key, mask);
-  const unsigned first_lane = lane_id() & 24u;
-  for (uint32_t p0 = 0; p0 <= mask; p0 += 8) {
-    const uint64_t v = sc.map_keys[(home + p0 + sub) & mask];
-    const unsigned hit = (__ballot_sync(tmask, v == key) & tmask) >> first_lane;
-    const unsigned emp = (__ballot_sync(tmask, v == kEmptyKey) & tmask) >> first_lane;
-    if (hit | emp) {  // the first position holding the key or free ends the probe
-      const int f = __ffs(hit | emp) - 1;
-      if (!((hit >> f) & 1u)) return kNone;
-      const uint32_t slot = (home + p0 + static_cast<uint32_t>(f)) & mask;
-      return sc.map_idx[slot] == static_cast<uint32_t>(i) + 1 ? slot : kNone;
-    }
   }
   return kNone;
 }
@@ -1130,18 +1108,19 @@ __device__ __forceinline__ void tile_probe_pair_many(const TableView& t, const u
   }
 }
 
-// Dual-mode pass 1 takes 32 consecutive keys per warp: the dedup lookup and
-// the per-key follow-up run one key per lane, so a warp keeps 32 keys'
-// accesses in flight; the two-line bucket probe runs on the warp's four
-// 8-lane tiles, each probing the keys of its own 8 lanes, kRouteKeysPerTile
-// at a time, and copying the input rows of the resident ones over their
-// table rows.  Result: the lane's own key's slot (or -1) and bucket.  `live`
-// selects the lanes whose key is probed.
+// Dual-mode pass 1 and assign take 32 consecutive keys per warp: the dedup
+// lookup and the per-key follow-up run one key per lane, so a warp keeps 32
+// keys' accesses in flight; the bucket probe (both candidate lines with
+// kPair) runs on the warp's four 8-lane tiles, each probing the keys of its
+// own 8 lanes, kRouteKeysPerTile at a time, and copying the input rows of
+// the resident ones over their table rows.  Result: the lane's own key's
+// slot (or -1) and bucket.  `live` selects the lanes whose key is probed.
 #ifndef HKV_ROUTE_KEYS_PER_TILE
 #define HKV_ROUTE_KEYS_PER_TILE 2
 #endif
 constexpr int kRouteKeysPerTile = HKV_ROUTE_KEYS_PER_TILE;
 
+template <bool kPair>
 __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k, uint64_t h,
                                                 uint64_t b1, uint64_t b2, bool live,
                                                 const float* values, uint64_t base, bool vec,
@@ -1164,13 +1143,20 @@ __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k,
       const int src = static_cast<int>(tile0) + r + u;
       kk[u] = __shfl_sync(0xFFFFFFFFu, k, src);
       c1[u] = __shfl_sync(0xFFFFFFFFu, b1, src);
-      c2[u] = __shfl_sync(0xFFFFFFFFu, b2, src);
+      c2[u] = kPair ? __shfl_sync(0xFFFFFFFFu, b2, src) : 0;
       pat[u] = __shfl_sync(0xFFFFFFFFu, my_pat, src);
       act[u] = __shfl_sync(0xFFFFFFFFu, live ? 1 : 0, src) != 0;
     }
     int slot[U];
     uint64_t bk[U];
-    tile_probe_pair_many<U>(t, c1, c2, kk, pat, act, sub, tmask, slot, bk);
+    if (kPair) {
+      tile_probe_pair_many<U>(t, c1, c2, kk, pat, act, sub, tmask, slot, bk);
+    } else {
+      uint64_t unused[U];
+      tile_probe_many<U>(t, c1, kk, pat, act, sub, tmask, slot, unused);
+#pragma unroll
+      for (int u = 0; u < U; ++u) bk[u] = c1[u];
+    }
     // resident keys: U row copies in flight
     float* dst[U];
     const float* src[U];
@@ -1196,7 +1182,7 @@ __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k,
 // Pass 1: resident keys update value (and score) in place; absent keys are
 // flagged in the dedup map (for the counts) and routed.
 #ifndef HKV_ASSIGN_MIN_BLOCKS
-#define HKV_ASSIGN_MIN_BLOCKS 6
+#define HKV_ASSIGN_MIN_BLOCKS 4
 #endif
 #ifndef HKV_ROUTE_MIN_BLOCKS
 #define HKV_ROUTE_MIN_BLOCKS 4
@@ -1219,7 +1205,7 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
     const uint64_t b1 = bucket_of_hash(t, h);
     const uint64_t b2 = bucket2_of(t, k, b1);
     uint64_t b;
-    const int slot = warp_probe_update(t, k, h, b1, b2, live, values, base, vec, b);
+    const int slot = warp_probe_update<true>(t, k, h, b1, b2, live, values, base, vec, b);
     if (!live) continue;
     sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
     const uint64_t inc = entry_inc(sc, ms);
@@ -1279,39 +1265,30 @@ __global__ void dual_finish_kernel(TableView t, UpsertScratch sc) {
 // ---------------------------------------------------------------------------
 // assign (updater) and erase (inserter).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel(TableView t, UpsertScratch sc, uint64_t n,
-                                                          const uint64_t* keys, const float* values,
-                                                          ScoreRule rule, bool keep_scores,
-                                                          bool vec) {
+template <bool kDual>
+__global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel(
+    TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
+    ScoreRule rule, bool keep_scores, bool vec) {
   const unsigned lane = lane_id();
-  const unsigned sub = lane & 7u;
-  const unsigned tmask = 0xFFu << (lane & 24u);
-  const uint64_t tiles = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
+  const uint64_t warps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   unsigned long long upd = 0;
-  for (uint64_t i = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; i < n;
-       i += tiles) {
-    const uint64_t k = keys[i];
-    if (is_reserved(k)) continue;
-    const uint32_t ms = tile_last_occurrence(sc, k, i, sub, tmask);
-    if (ms == kNone) continue;
+  for (uint64_t base = ((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 32;
+       base < n; base += warps * 32) {
+    const uint64_t i = base + lane;
+    const uint64_t k = i < n ? keys[i] : kEmptyKey;
+    const uint32_t ms = i < n && !is_reserved(k) ? map_last_occurrence(sc, k, i) : kNone;
+    const bool live = ms != kNone;  // the key's last occurrence in the batch
     const uint64_t h = hash64(k);
-    const uint32_t pat = digest_of_hash(h) * 0x01010101u;
-    uint64_t b = bucket_of_hash(t, h);
-    int slot = tile_probe<true>(t, b, k, pat, sub, tmask);
-    if (t.dual && slot < 0) {
-      b = bucket2_of(t, k, b);
-      slot = tile_probe<true>(t, b, k, pat, sub, tmask);
+    const uint64_t b1 = bucket_of_hash(t, h);
+    uint64_t b;
+    const int slot = warp_probe_update<kDual>(t, k, h, b1, kDual ? bucket2_of(t, k, b1) : b1,
+                                              live, values, base, vec, b);
+    if (!live || slot < 0) continue;
+    if (!keep_scores) {
+      uint64_t* sp = score_at(t, b * kSlots + static_cast<uint64_t>(slot));
+      *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
     }
-    if (slot < 0) continue;
-    const uint64_t row = b * kSlots + static_cast<uint64_t>(slot);
-    tile_copy_row(row_ptr(t, row), values + i * t.dim, t.dim, sub, vec, true);
-    if (sub == 0) {
-      if (!keep_scores) {
-        uint64_t* sp = score_at(t, row);
-        *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
-      }
-      ++upd;
-    }
+    ++upd;
   }
   warp_add(&t.stats->updated, upd);
 }
@@ -1561,8 +1538,12 @@ cudaError_t launch_assign(const TableView& t, const UpsertScratch& s, uint64_t n
   const bool vec = (t.dim % 4 == 0) && ((reinterpret_cast<uintptr_t>(values) & 15) == 0);
   dedup_insert_kernel<<<grid_for(n), kThreads, 0, st>>>(s, n, keys, rule.lfu() ? rule.in : nullptr,
                                                          t.stats);
-  assign_kernel<<<grid_for(n * 8), kThreads, 0, st>>>(t, s, n, keys, values, rule, keep_scores,
-                                                       vec);
+  if (t.dual)
+    assign_kernel<true><<<grid_for(n, HKV_ASSIGN_MIN_BLOCKS), kThreads, 0, st>>>(
+        t, s, n, keys, values, rule, keep_scores, vec);
+  else
+    assign_kernel<false><<<grid_for(n, HKV_ASSIGN_MIN_BLOCKS), kThreads, 0, st>>>(
+        t, s, n, keys, values, rule, keep_scores, vec);
   return cudaGetLastError();
 }
 
