@@ -108,15 +108,15 @@ def upsert_access_floor(n, dim, rows_written, buckets_touched, rates, hbm_gbs):
 
 # DRAM bytes (read + write) of one launch, from an ncu capture of the timed
 # region of `python bench.py --skip-sweep --no-cpu-baseline --steps 3
-# --warmup 3` (profiles/find_kernel_c2.md, profiles/upsert_kernels_c2.md),
+# --warmup 3` (the mean of its 3 launches, profiles/launches_c2_step.md),
 # valid only while the kernel's sources are the ones captured (sha256 prefix
 # over the listed files).
 NCU_TRAFFIC = {
-    "find_kernel": {"bytes": 164755712 + 69267968, "sources": ("find.cu", "common.cuh", "launch.h"),
-                    "sha256": "2f71ef7c08587846"},
-    "upsert_single_kernel": {"bytes": 180330496 + 61313536,
+    "find_kernel": {"bytes": 162568107 + 65613824, "sources": ("find.cu", "common.cuh", "launch.h"),
+                    "sha256": "e4780e0d8a6314bd"},
+    "upsert_single_kernel": {"bytes": 178647979 + 55424768,
                              "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "9e6740b699809826"},
+                             "sha256": "1040537868e847d3"},
 }
 
 
