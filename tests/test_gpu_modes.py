@@ -252,3 +252,53 @@ def test_roles_across_streams(hkv, oracle_mod):
         assert np.array_equal(u64(gs), os_)
         o.assign(a, av, None)
     assert_same_state(t, o)
+
+
+@pytest.mark.parametrize("with_scores", [True, False])
+def test_dual_assign_exact(hkv, with_scores):
+    """assign on a full dual table, batches with resident keys, absent keys
+    and repeats: placement is untouched (the export slot of every key stays),
+    a resident key takes the values (and score, when given) of its last
+    occurrence, everything else keeps its bytes, absent keys stay absent."""
+    B, dim = 200, 12
+    cap = B * 128
+    t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_DUAL)
+    keys = wl.unique_keys(95, 2 * cap)
+    scores = wl.stream(96, keys.size) >> np.uint64(2)
+    for lo in range(0, keys.size, 5000):
+        k = keys[lo:lo + 5000]
+        t.insert_or_assign(dkeys(k), dvals(wl.key_values(k, dim, salt=3)), dkeys(scores[lo:lo + 5000]))
+    rng = np.random.default_rng(97)
+
+    def state():  # sorted by key (export order is unspecified)
+        k, v, s = table_state(t)
+        o = np.argsort(k)
+        return k[o], v[o], s[o]
+
+    for r in range(4):
+        k0, v0, s0 = state()
+        pos = {x: i for i, x in enumerate(k0.tolist())}
+        slots0 = _slots_state(t)
+        absent = np.setdiff1d(keys, k0)
+        batch = np.concatenate([rng.choice(k0, 3000), rng.choice(absent, 1000)])
+        rng.shuffle(batch)
+        vals = rng.standard_normal((batch.size, dim)).astype(np.float32)
+        sc = wl.stream(98 + r, batch.size) >> np.uint64(2)
+        t.reset_op_counts()
+        t.assign(dkeys(batch), dvals(vals), dkeys(sc) if with_scores else None)
+        want_v, want_s = v0.copy(), s0.copy()
+        for i, x in enumerate(batch.tolist()):  # in batch order: the last occurrence wins
+            j = pos.get(x)
+            if j is not None:
+                want_v[j] = vals[i]
+                if with_scores:
+                    want_s[j] = sc[i]
+        k1, v1, s1 = state()
+        assert np.array_equal(k1, k0)
+        slots1 = _slots_state(t)  # every key still in the same bucket
+        assert np.array_equal(slots1[0], slots0[0]) and np.array_equal(slots1[2], slots0[2])
+        assert np.array_equal(v1.view(np.uint32), want_v.view(np.uint32))
+        assert np.array_equal(s1, want_s)
+        assert t.op_counts()["updated"] == len({x for x in batch.tolist() if x in pos})
+        assert int(t.contains(dkeys(absent)).sum().item()) == 0
+    t.close()
