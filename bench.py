@@ -116,7 +116,7 @@ NCU_TRAFFIC = {
                     "sha256": "e4780e0d8a6314bd"},
     "upsert_single_kernel": {"bytes": 178647979 + 55424768,
                              "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "1040537868e847d3"},
+                             "sha256": "2cca58e34ab6bb44"},
 }
 
 

@@ -24,11 +24,12 @@
 // on thread scheduling, so it equals the oracle's serial result exactly.
 //
 // Dual mode couples two buckets per key.  The batch is de-duplicated in a
-// scratch map; a tile kernel updates resident keys in place and routes each
-// absent key to one of its buckets by Algorithm 3's rules on per-bucket
-// summaries; the same bucket kernel then places every bucket's routed keys;
-// keys that pass displaces are routed once more and placed in a second pass.
-// No locks: every bucket still has one owner per pass.
+// scratch map; a route kernel (32 keys per warp, both candidate lines probed
+// by 8-lane tiles) updates resident keys in place and routes each absent key
+// to one of its buckets by Algorithm 3's rules on per-bucket summaries; the
+// same bucket kernel then places every bucket's routed keys; keys that pass
+// displaces are routed once more and placed in a second pass.  No locks:
+// every bucket still has one owner per pass.
 #include <cstddef>
 
 #include "launch.h"
