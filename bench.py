@@ -112,11 +112,11 @@ def upsert_access_floor(n, dim, rows_written, buckets_touched, rates, hbm_gbs):
 # valid only while the kernel's sources are the ones captured (sha256 prefix
 # over the listed files).
 NCU_TRAFFIC = {
-    "find_kernel": {"bytes": 162568107 + 65613824, "sources": ("find.cu", "common.cuh", "launch.h"),
+    "find_kernel": {"bytes": 162563669 + 65430016, "sources": ("find.cu", "common.cuh", "launch.h"),
                     "sha256": "e4780e0d8a6314bd"},
-    "upsert_single_kernel": {"bytes": 178647979 + 55424768,
+    "upsert_single_kernel": {"bytes": 178632192 + 55387307,
                              "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "2cca58e34ab6bb44"},
+                             "sha256": "cde1413d76b7a85b"},
 }
 
 
@@ -480,28 +480,32 @@ def run_gpu(args):
         bi = hk[0].numel() * 8 + hv[0].numel() * 4 + hq[0].numel() * 8
         bo = hvo[0].numel() * 4 + hfo[0].numel() + hso[0].numel() * 8
         # The host link alone: the same uploads and downloads with no table
-        # work between them, both directions on their own streams.
-        torch.cuda.synchronize()
-        a.record(stream)
-        up_s.wait_event(a)
-        dn_s.wait_event(a)
-        for s in range(ne):
-            i = s % 2
-            with torch.cuda.stream(up_s):
-                dk_[i].copy_(hk[i], non_blocking=True)
-                dv_[i].copy_(hv[i], non_blocking=True)
-                dq_[i].copy_(hq[i], non_blocking=True)
-            with torch.cuda.stream(dn_s):
-                hvo[i].copy_(ov_[i], non_blocking=True)
-                hfo[i].copy_(of_[i], non_blocking=True)
-                hso[i].copy_(os_[i], non_blocking=True)
-        for s_ in (up_s, dn_s):
-            x = torch.cuda.Event()
-            x.record(s_)
-            stream.wait_event(x)
-        b.record(stream)
-        b.synchronize()
-        link_total = a.elapsed_time(b) * 1e-3
+        # work between them, both directions on their own streams; the best
+        # of 3 runs (the link is shared with the machine's other work).
+        link_runs = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a.record(stream)
+            up_s.wait_event(a)
+            dn_s.wait_event(a)
+            for s in range(ne):
+                i = s % 2
+                with torch.cuda.stream(up_s):
+                    dk_[i].copy_(hk[i], non_blocking=True)
+                    dv_[i].copy_(hv[i], non_blocking=True)
+                    dq_[i].copy_(hq[i], non_blocking=True)
+                with torch.cuda.stream(dn_s):
+                    hvo[i].copy_(ov_[i], non_blocking=True)
+                    hfo[i].copy_(of_[i], non_blocking=True)
+                    hso[i].copy_(os_[i], non_blocking=True)
+            for s_ in (up_s, dn_s):
+                x = torch.cuda.Event()
+                x.record(s_)
+                stream.wait_event(x)
+            b.record(stream)
+            b.synchronize()
+            link_runs.append(a.elapsed_time(b) * 1e-3)
+        link_total = min(link_runs)
         e2e = {"value": 2 * BATCH * ne * world / e_total / 1e9, "unit": "B-KV/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "steps": ne, "overlap": "uploads and downloads on their own streams, double buffered",

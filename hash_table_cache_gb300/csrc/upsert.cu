@@ -1113,20 +1113,23 @@ __device__ __forceinline__ void tile_probe_pair_many(const TableView& t, const u
 // lookup and the per-key follow-up run one key per lane, so a warp keeps 32
 // keys' accesses in flight; the bucket probe (both candidate lines with
 // kPair) runs on the warp's four 8-lane tiles, each probing the keys of its
-// own 8 lanes, kRouteKeysPerTile at a time, and copying the input rows of
-// the resident ones over their table rows.  Result: the lane's own key's
+// own 8 lanes, U at a time, and copying the input rows of the resident ones
+// over their table rows.  Result: the lane's own key's
 // slot (or -1) and bucket.  `live` selects the lanes whose key is probed.
 #ifndef HKV_ROUTE_KEYS_PER_TILE
-#define HKV_ROUTE_KEYS_PER_TILE 2
+#define HKV_ROUTE_KEYS_PER_TILE 1
+#endif
+#ifndef HKV_ASSIGN_KEYS_PER_TILE
+#define HKV_ASSIGN_KEYS_PER_TILE 1
 #endif
 constexpr int kRouteKeysPerTile = HKV_ROUTE_KEYS_PER_TILE;
+constexpr int kAssignKeysPerTile = HKV_ASSIGN_KEYS_PER_TILE;
 
-template <bool kPair>
+template <bool kPair, int U>
 __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k, uint64_t h,
                                                 uint64_t b1, uint64_t b2, bool live,
                                                 const float* values, uint64_t base, bool vec,
                                                 uint64_t& bkt) {
-  constexpr int U = kRouteKeysPerTile;
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tile0 = lane & 24u;
@@ -1183,10 +1186,10 @@ __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k,
 // Pass 1: resident keys update value (and score) in place; absent keys are
 // flagged in the dedup map (for the counts) and routed.
 #ifndef HKV_ASSIGN_MIN_BLOCKS
-#define HKV_ASSIGN_MIN_BLOCKS 4
+#define HKV_ASSIGN_MIN_BLOCKS 6
 #endif
 #ifndef HKV_ROUTE_MIN_BLOCKS
-#define HKV_ROUTE_MIN_BLOCKS 4
+#define HKV_ROUTE_MIN_BLOCKS 6
 #endif
 __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
@@ -1206,7 +1209,8 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
     const uint64_t b1 = bucket_of_hash(t, h);
     const uint64_t b2 = bucket2_of(t, k, b1);
     uint64_t b;
-    const int slot = warp_probe_update<true>(t, k, h, b1, b2, live, values, base, vec, b);
+    const int slot =
+        warp_probe_update<true, kRouteKeysPerTile>(t, k, h, b1, b2, live, values, base, vec, b);
     if (!live) continue;
     sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
     const uint64_t inc = entry_inc(sc, ms);
@@ -1282,8 +1286,8 @@ __global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel
     const uint64_t h = hash64(k);
     const uint64_t b1 = bucket_of_hash(t, h);
     uint64_t b;
-    const int slot = warp_probe_update<kDual>(t, k, h, b1, kDual ? bucket2_of(t, k, b1) : b1,
-                                              live, values, base, vec, b);
+    const int slot = warp_probe_update<kDual, kAssignKeysPerTile>(
+        t, k, h, b1, kDual ? bucket2_of(t, k, b1) : b1, live, values, base, vec, b);
     if (!live || slot < 0) continue;
     if (!keep_scores) {
       uint64_t* sp = score_at(t, b * kSlots + static_cast<uint64_t>(slot));
