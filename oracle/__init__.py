@@ -13,7 +13,7 @@ of ``hkv_oracle.cpp``.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against brute force, closed forms and the paper's special cases, except the
-hash (``hash64``), which the paper names only as "derived from Murmur3"; it is
+hash (``hash64``), which the paper names only as a Murmur3 derivative; it is
 pinned by bijectivity and avalanche statistics only.
 """
 from __future__ import annotations

@@ -15,7 +15,7 @@
 //
 // Readings taken where the paper is silent or inconsistent (each one is also
 // listed in the design notes of the repository):
-//  R1 hash: the paper says only "derived from Murmur3"; we use the 64-bit
+//  R1 hash: the paper names it only as a Murmur3 derivative; we use the 64-bit
 //     MurmurHash3 finalizer (Appleby, public domain) as H(k).
 //  R2 bucket b1 = H(k) mod B.  Dual mode: b2 = H(k ^ 0x9E3779B97F4A7C15) mod B,
 //     and b2 = (b1 + 1) mod B when the two coincide.

@@ -15,7 +15,7 @@ MASK = (1 << 64) - 1
 
 
 # --------------------------------------------------------------------------
-# Hash: the paper only says "derived from Murmur3" (HKV §3.1/§3.2), so its
+# Hash: the paper names it only as a Murmur3 derivative (HKV §3.1/§3.2), so its
 # exact values are unpinned; we pin the properties of the chosen finalizer.
 # --------------------------------------------------------------------------
 def test_hash_fixes_zero(oracle_mod):
