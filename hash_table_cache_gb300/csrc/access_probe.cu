@@ -6,18 +6,24 @@
 // streaming bandwidth.  This probe measures what the GPU sustains for that
 // access pattern: reads of `granule` bytes at uniformly random, granule-
 // aligned offsets of a buffer far larger than L2.  Granules of 32 bytes are
-// read one per lane; larger granules by 8-lane tiles, 16 bytes per lane, the
-// way the table kernels read digest lines and value rows.  Each thread or
-// tile keeps kInFlight independent reads outstanding.
+// read one per lane; larger granules by 8-lane tiles, 16 bytes per lane per
+// 128 bytes, the way the table kernels read digest lines and value rows.
+// Each thread or tile keeps D independent reads outstanding (D = 1..16), and
+// the grid holds a chosen number of 256-thread blocks per SM, so the rate can
+// be swept over the number of reads in flight until it stops growing.
 //
-// Offsets come from a fixed integer mix of (thread, iteration) reduced modulo
-// the number of granules, so every read stays inside the buffer.
+// The buffer size is a power of two and offsets are a fixed integer mix of
+// (thread, iteration) masked to the granule count, so every read stays inside
+// the buffer and the address arithmetic costs a few instructions.
+//
+// A second probe measures the host link the way tiered mode uses it: SM loads
+// and stores (not copy-engine transfers) of 16-byte vectors over mapped
+// pinned host memory, either streaming (consecutive addresses) or as random
+// rows of `granule` bytes.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace {
-
-constexpr int kInFlight = 4;
 
 __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   x ^= x >> 33;
@@ -28,59 +34,172 @@ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   return x;
 }
 
-__global__ void sector_reads(const uint8_t* buf, uint64_t granules, uint64_t iters,
+template <int D>
+__global__ void sector_reads(const uint8_t* buf, uint64_t mask, uint32_t iters,
                              unsigned long long* sink) {
   const uint64_t tid = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x;
   unsigned long long acc = 0;
-  for (uint64_t it = 0; it < iters; ++it) {
-    unsigned long long v[kInFlight];
+  for (uint32_t it = 0; it < iters; ++it) {
+    unsigned long long v[D];
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) {
-      const uint64_t g = mix64(tid * 0x9E3779B97F4A7C15ull + it * kInFlight + u) % granules;
+    for (int u = 0; u < D; ++u) {
+      const uint64_t g = mix64(tid * 0x9E3779B97F4A7C15ull + it * D + u) & mask;
       v[u] = __ldcg(reinterpret_cast<const unsigned long long*>(buf + g * 32));
     }
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) acc ^= v[u];
+    for (int u = 0; u < D; ++u) acc ^= v[u];
   }
   if (acc == 0x5EEDull) *sink = acc;  // keeps the loads
 }
 
-__global__ void line_reads(const uint8_t* buf, uint64_t granules, uint32_t granule, uint64_t iters,
+// Tile reads: granule = 128 * C bytes is read as C 16-byte loads per lane
+// (granules of 48..112 bytes: lanes past the end stay idle).
+template <int D, int C>
+__global__ void line_reads(const uint8_t* buf, uint64_t mask, uint32_t granule, uint32_t iters,
                            unsigned long long* sink) {
   const uint64_t tile = (blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x) >> 3;
   const uint32_t sub = threadIdx.x & 7u;
+  const uint32_t vecs = granule / 16;
   uint32_t acc = 0;
-  for (uint64_t it = 0; it < iters; ++it) {
-    uint4 v[kInFlight];
+  for (uint32_t it = 0; it < iters; ++it) {
+    uint4 v[D][C];
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) {
-      v[u] = make_uint4(0, 0, 0, 0);
-      const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it * kInFlight + u) % granules;
+    for (int u = 0; u < D; ++u) {
+      const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it * D + u) & mask;
       const uint8_t* p = buf + g * granule;
-      for (uint32_t c = sub; c < granule / 16; c += 8) {
-        const uint4 w = __ldcg(reinterpret_cast<const uint4*>(p + 16 * c));
-        v[u].x ^= w.x;
-        v[u].w ^= w.w;
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        const uint32_t q = sub + 8u * c;
+        v[u][c] = q < vecs ? __ldcg(reinterpret_cast<const uint4*>(p + 16 * q))
+                           : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) acc ^= v[u].x ^ v[u].w;
+    for (int u = 0; u < D; ++u)
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc ^= v[u][c].x ^ v[u][c].w;
   }
   if (acc == 0x5EEDu) *sink = acc;
 }
+
+template <int D>
+cudaError_t launch_reads(uint32_t granule, const uint8_t* buf, uint64_t mask, unsigned grid,
+                         uint32_t iters, unsigned long long* sink) {
+  if (granule == 32)
+    sector_reads<D><<<grid, 256>>>(buf, mask, iters, sink);
+  else if (granule <= 128)
+    line_reads<D, 1><<<grid, 256>>>(buf, mask, granule, iters, sink);
+  else if (granule <= 256)
+    line_reads<D, 2><<<grid, 256>>>(buf, mask, granule, iters, sink);
+  else
+    line_reads<D, 4><<<grid, 256>>>(buf, mask, granule, iters, sink);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_depth(int depth, uint32_t granule, const uint8_t* buf, uint64_t mask,
+                         unsigned grid, uint32_t iters, unsigned long long* sink) {
+  switch (depth) {
+    case 1: return launch_reads<1>(granule, buf, mask, grid, iters, sink);
+    case 2: return launch_reads<2>(granule, buf, mask, grid, iters, sink);
+    case 4: return launch_reads<4>(granule, buf, mask, grid, iters, sink);
+    case 8: return launch_reads<8>(granule, buf, mask, grid, iters, sink);
+    default: return launch_reads<16>(granule, buf, mask, grid, iters, sink);
+  }
+}
+
+// Host-link probe kernels: 16-byte SM loads / stores over mapped host memory.
+// Streaming: the grid walks the buffer in consecutive 16-byte vectors.
+__global__ void host_stream_read(const uint4* p, uint64_t nvec, unsigned long long* sink) {
+  uint32_t acc = 0;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < nvec;
+       i += stride) {
+    const uint4 w = __ldcg(p + i);
+    acc ^= w.x ^ w.w;
+  }
+  if (acc == 0x5EEDu) *sink = acc;
+}
+
+__global__ void host_stream_write(uint4* p, uint64_t nvec) {
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < nvec;
+       i += stride)
+    p[i] = make_uint4(static_cast<uint32_t>(i), 1u, 2u, 3u);
+}
+
+// Random rows of `granule` bytes (a multiple of 16, at most 512), one row per
+// 8-lane tile at a time, 4 rows in flight per tile; `rows` is a power of two.
+__global__ void host_row_read(const uint8_t* p, uint64_t row_mask, uint32_t granule,
+                              uint32_t iters, unsigned long long* sink) {
+  const uint64_t tile = (blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x) >> 3;
+  const uint32_t sub = threadIdx.x & 7u;
+  const uint32_t vecs = granule / 16;
+  uint32_t acc = 0;
+  for (uint32_t it = 0; it < iters; ++it) {
+    uint4 v[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it * 4 + u) & row_mask;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t q = sub + 8u * c;
+        v[u][c] = q < vecs ? __ldcg(reinterpret_cast<const uint4*>(p + g * granule + 16 * q))
+                           : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc ^= v[u][c].x ^ v[u][c].w;
+  }
+  if (acc == 0x5EEDu) *sink = acc;
+}
+
+__global__ void host_row_write(uint8_t* p, uint64_t row_mask, uint32_t granule, uint32_t iters) {
+  const uint64_t tile = (blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x) >> 3;
+  const uint32_t sub = threadIdx.x & 7u;
+  const uint32_t vecs = granule / 16;
+  for (uint32_t it = 0; it < iters; ++it) {
+    const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it) & row_mask;
+    for (uint32_t q = sub; q < vecs; q += 8)
+      *reinterpret_cast<uint4*>(p + g * granule + 16 * q) = make_uint4(it, 1u, 2u, 3u);
+  }
+}
+
+bool pow2(uint64_t x) { return x && !(x & (x - 1)); }
+
+struct Timer {
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaError_t init() {
+    cudaError_t e = cudaEventCreate(&a);
+    return e == cudaSuccess ? cudaEventCreate(&b) : e;
+  }
+  ~Timer() {
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+  }
+};
 
 }  // namespace
 
 extern "C" {
 
 // Measures random reads of `granule` bytes (32, or a multiple of 16 from 48
-// to 4096) over a freshly allocated device buffer of `buffer_bytes` on the
-// current device.  Writes the reads per second to *reads_per_s.  Returns 0,
+// to 512) over a freshly allocated device buffer of `buffer_bytes` (a power
+// of two, at least 64 MiB) on the current device, with `in_flight` (1, 2, 4,
+// 8 or 16) independent reads outstanding per thread (32-byte granules) or per
+// 8-lane tile (larger granules) and `blocks_per_sm` (1..8) blocks of 256
+// threads per SM.  Writes the reads per second to *reads_per_s.  Returns 0,
 // -1 on bad arguments, or the CUDA error code.  Allocates and frees its
 // buffer; synchronises the device.
-int hkv_probe_random_reads(uint32_t granule, uint64_t buffer_bytes, double* reads_per_s) {
-  const bool ok_granule = granule == 32 || (granule % 16 == 0 && granule >= 48 && granule <= 4096);
-  if (!reads_per_s || !ok_granule || buffer_bytes < (64ull << 20)) return -1;
+int hkv_probe_random_reads_at(uint32_t granule, uint64_t buffer_bytes, int in_flight,
+                              int blocks_per_sm, double* reads_per_s) {
+  const bool ok_granule = granule == 32 || (granule % 16 == 0 && granule >= 48 && granule <= 512);
+  const bool ok_depth = in_flight == 1 || in_flight == 2 || in_flight == 4 || in_flight == 8 ||
+                        in_flight == 16;
+  if (!reads_per_s || !ok_granule || !ok_depth || blocks_per_sm < 1 || blocks_per_sm > 8 ||
+      !pow2(buffer_bytes) || buffer_bytes < (64ull << 20))
+    return -1;
   uint8_t* buf = nullptr;
   unsigned long long* sink = nullptr;
   cudaError_t e = cudaMalloc(&buf, buffer_bytes);
@@ -89,35 +208,101 @@ int hkv_probe_random_reads(uint32_t granule, uint64_t buffer_bytes, double* read
   int dev = 0, sms = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaEvent_t a = nullptr, b = nullptr;
-  if (e == cudaSuccess) e = cudaEventCreate(&a);
-  if (e == cudaSuccess) e = cudaEventCreate(&b);
+  Timer tm;
+  if (e == cudaSuccess) e = tm.init();
   if (e == cudaSuccess) {
-    const unsigned threads = 256, grid = static_cast<unsigned>(sms) * 8;
-    const uint64_t granules = buffer_bytes / granule;
-    const uint64_t iters = 32;
-    auto launch = [&]() {
-      if (granule == 32)
-        sector_reads<<<grid, threads>>>(buf, granules, iters, sink);
-      else
-        line_reads<<<grid, threads>>>(buf, granules, granule, iters, sink);
-    };
-    launch();  // warm-up
-    cudaEventRecord(a);
-    launch();
-    cudaEventRecord(b);
-    e = cudaEventSynchronize(b);
-    float ms = 0.f;
-    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
-    if (e == cudaSuccess) e = cudaGetLastError();
+    const unsigned grid = static_cast<unsigned>(sms) * blocks_per_sm;
+    // power-of-two granule count: the largest power of two of granules that
+    // fits the buffer
+    uint64_t granules = 1;
+    while (granules * 2 * granule <= buffer_bytes) granules *= 2;
+    const uint64_t mask = granules - 1;
     const double lanes_per_read = granule == 32 ? 1.0 : 8.0;
-    const double reads = static_cast<double>(grid) * threads / lanes_per_read * iters * kInFlight;
-    if (e == cudaSuccess) *reads_per_s = ms > 0.f ? reads / (ms * 1e-3) : 0.0;
+    // about 2^24 reads per launch, whatever the depth and the grid
+    const double per_iter = static_cast<double>(grid) * 256 / lanes_per_read * in_flight;
+    uint32_t iters = static_cast<uint32_t>((1 << 24) / per_iter);
+    if (iters < 4) iters = 4;
+    e = launch_depth(in_flight, granule, buf, mask, grid, iters, sink);  // warm-up
+    if (e == cudaSuccess) e = cudaEventRecord(tm.a);
+    if (e == cudaSuccess) e = launch_depth(in_flight, granule, buf, mask, grid, iters, sink);
+    if (e == cudaSuccess) e = cudaEventRecord(tm.b);
+    if (e == cudaSuccess) e = cudaEventSynchronize(tm.b);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, tm.a, tm.b);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) *reads_per_s = ms > 0.f ? per_iter * iters / (ms * 1e-3) : 0.0;
   }
-  if (a) cudaEventDestroy(a);
-  if (b) cudaEventDestroy(b);
   if (buf) cudaFree(buf);
   if (sink) cudaFree(sink);
+  return e == cudaSuccess ? 0 : static_cast<int>(e);
+}
+
+// The earlier form: 4 reads in flight, 8 blocks per SM.
+int hkv_probe_random_reads(uint32_t granule, uint64_t buffer_bytes, double* reads_per_s) {
+  uint64_t p = 1;
+  while (p * 2 <= buffer_bytes) p *= 2;
+  return hkv_probe_random_reads_at(granule, p, 4, 8, reads_per_s);
+}
+
+// Measures SM access to mapped pinned host memory, the path tiered mode's
+// value rows take.  kind: 0 = streaming 16-byte reads, 1 = streaming 16-byte
+// writes, 2 = random reads of `granule`-byte rows, 3 = random writes of
+// `granule`-byte rows (granule a multiple of 16, 16..512).  `buffer_bytes` is
+// a power of two of at least 64 MiB; the host buffer is allocated with
+// cudaHostAllocMapped and freed before return.  Writes bytes per second to
+// *bytes_per_s.  Returns 0, -1 on bad arguments, or the CUDA error code.
+// Synchronises the device.
+int hkv_probe_host_link(int kind, uint32_t granule, uint64_t buffer_bytes, double* bytes_per_s) {
+  if (!bytes_per_s || kind < 0 || kind > 3 || !pow2(buffer_bytes) || buffer_bytes < (64ull << 20))
+    return -1;
+  if (kind >= 2 && (granule % 16 != 0 || granule < 16 || granule > 512)) return -1;
+  void* host = nullptr;
+  uint8_t* dp = nullptr;
+  unsigned long long* sink = nullptr;
+  cudaError_t e = cudaHostAlloc(&host, buffer_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dp), host, 0);
+  if (e == cudaSuccess) e = cudaMalloc(&sink, sizeof(unsigned long long));
+  int dev = 0, sms = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  Timer tm;
+  if (e == cudaSuccess) e = tm.init();
+  if (e == cudaSuccess) {
+    const unsigned grid = static_cast<unsigned>(sms) * 4;
+    const uint64_t nvec = buffer_bytes / 16;
+    uint64_t rows = 1;
+    if (kind >= 2)
+      while (rows * 2 * granule <= buffer_bytes) rows *= 2;
+    const uint64_t tiles = static_cast<uint64_t>(grid) * 256 / 8;
+    // random kinds: about buffer_bytes of rows per launch
+    uint32_t iters = kind >= 2 ? static_cast<uint32_t>(buffer_bytes / granule / tiles) : 0;
+    if (kind == 2) iters = (iters + 3) / 4;  // 4 rows per iteration
+    if (kind >= 2 && iters < 1) iters = 1;
+    double bytes = 0;
+    auto launch = [&]() {
+      switch (kind) {
+        case 0: host_stream_read<<<grid, 256>>>(reinterpret_cast<const uint4*>(dp), nvec, sink);
+                bytes = static_cast<double>(buffer_bytes); break;
+        case 1: host_stream_write<<<grid, 256>>>(reinterpret_cast<uint4*>(dp), nvec);
+                bytes = static_cast<double>(buffer_bytes); break;
+        case 2: host_row_read<<<grid, 256>>>(dp, rows - 1, granule, iters, sink);
+                bytes = static_cast<double>(tiles) * iters * 4 * granule; break;
+        default: host_row_write<<<grid, 256>>>(dp, rows - 1, granule, iters);
+                 bytes = static_cast<double>(tiles) * iters * granule; break;
+      }
+      return cudaGetLastError();
+    };
+    e = launch();  // warm-up
+    if (e == cudaSuccess) e = cudaEventRecord(tm.a);
+    if (e == cudaSuccess) e = launch();
+    if (e == cudaSuccess) e = cudaEventRecord(tm.b);
+    if (e == cudaSuccess) e = cudaEventSynchronize(tm.b);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, tm.a, tm.b);
+    if (e == cudaSuccess) *bytes_per_s = ms > 0.f ? bytes / (ms * 1e-3) : 0.0;
+  }
+  if (sink) cudaFree(sink);
+  if (host) cudaFreeHost(host);
   return e == cudaSuccess ? 0 : static_cast<int>(e);
 }
 
