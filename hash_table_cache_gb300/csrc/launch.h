@@ -34,6 +34,7 @@ struct UpsertScratch {
   uint32_t* stage_idx;
   uint32_t* stage_bkt;
   uint64_t* stage_inc;
+  size_t bytes;         // bytes of the allocation the carving uses
 };
 
 // What a call needs scratch for.

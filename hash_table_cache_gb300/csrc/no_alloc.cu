@@ -16,7 +16,9 @@
 // module keeps its HKV_NOALLOC_SCRATCH_BYTES until the process exits.  Host
 // code cannot use the array's name as a device address, so the first call on
 // a device (with that device current) asks the runtime for the address with
-// cudaGetSymbolAddress and caches it per device.
+// cudaGetSymbolAddress and caches it per device.  The cache is not refreshed:
+// after cudaDeviceReset the module may be loaded at another address, so the
+// header tells callers not to use this function on a reset device.
 #include <mutex>
 
 #include "hkv.h"

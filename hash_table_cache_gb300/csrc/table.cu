@@ -70,6 +70,18 @@ class RoleTracker {
     return cudaSuccess;
   }
 
+  // Create k events ahead of use, so that later calls find them in the free
+  // list.
+  cudaError_t reserve(int k) {
+    for (int i = 0; i < k; ++i) {
+      cudaEvent_t ev = nullptr;
+      cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+      free_.push_back(ev);
+    }
+    return cudaSuccess;
+  }
+
   // Block the host until every recorded call has finished.
   cudaError_t wait_all() {
     cudaError_t e = cudaSuccess;
@@ -188,19 +200,25 @@ hkv::ScoreRule take_rule(hkv_table* t, const uint64_t* scores) {
   return r;
 }
 
-// Common frame of a batched call: lock, select the device, order by role,
-// run `body`, record the role event.
+// Order a call by role: wait for the conflicting calls, run `body`, record
+// the call's role event.  The caller holds the table lock and has selected
+// the device.
 template <class F>
-hkv_status run_call(hkv_table* t, Role r, void* stream, F&& body) {
-  std::lock_guard<std::mutex> lk(t->mu);
-  DeviceGuard g(t->device);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+hkv_status run_ordered(hkv_table* t, Role r, cudaStream_t s, F&& body) {
   cudaError_t e = t->roles.before(r, s);
   if (e != cudaSuccess) return from_cuda(e);
   hkv_status st = body(s);
   e = t->roles.after(r, s, t->aux);
   if (st != HKV_OK) return st;
   return from_cuda(e);
+}
+
+// Common frame of a batched call: lock, select the device, order by role.
+template <class F>
+hkv_status run_call(hkv_table* t, Role r, void* stream, F&& body) {
+  std::lock_guard<std::mutex> lk(t->mu);
+  DeviceGuard g(t->device);
+  return run_ordered(t, r, static_cast<cudaStream_t>(stream), body);
 }
 
 }  // namespace
@@ -220,15 +238,21 @@ int NoAllocAccess::run(hkv_table* t, uint64_t n, const uint64_t* keys, const flo
   void* mem = nullptr;
   cudaError_t e = get_scratch(t->device, &mem);
   if (e != cudaSuccess) return from_cuda(e);
+  UpsertScratch sc{};
+  if (n) {
+    sc = carve_upsert_scratch(mem, n, t->v.num_buckets, kind, lfu_policy(t));
+    // the carving itself must stay inside the array, whatever the formula
+    // above says
+    if (sc.bytes > HKV_NOALLOC_SCRATCH_BYTES) return HKV_ERR_INVALID;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = t->roles.before(Role::kInserter, s);  // waits only: records no event
-  if (e != cudaSuccess) return from_cuda(e);
-  const ScoreRule rule = take_rule(t, scores);
-  if (n == 0) return HKV_OK;
-  UpsertScratch sc = carve_upsert_scratch(mem, n, t->v.num_buckets, kind, lfu_policy(t));
-  e = clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
-  if (e == cudaSuccess) e = launch_upsert(t->v, sc, n, keys, values, rule, s);
-  return from_cuda(e);
+  return run_ordered(t, Role::kInserter, s, [&](cudaStream_t) -> hkv_status {
+    const ScoreRule rule = take_rule(t, scores);
+    if (n == 0) return HKV_OK;
+    cudaError_t f = clear_upsert_scratch(sc, t->v.num_buckets, kind, s);
+    if (f == cudaSuccess) f = launch_upsert(t->v, sc, n, keys, values, rule, s);
+    return from_cuda(f);
+  });
 }
 
 }  // namespace hkv
@@ -284,6 +308,9 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
       e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&v.values_host), t->host_slab, 0);
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&t->aux, cudaStreamNonBlocking);
+  // role events for the first calls (a call reuses the events of the calls
+  // an inserter has retired)
+  if (e == cudaSuccess) e = t->roles.reserve(4);
   if (e == cudaSuccess) {
     cudaMemPoolProps props{};
     props.allocType = cudaMemAllocationTypePinned;
@@ -558,6 +585,8 @@ hkv_status hkv_get_info(hkv_table* t, hkv_info* out) {
   out->dim = t->v.dim;
   out->mode = t->mode;
   out->device = t->device;
+  out->hbm_values_addr = reinterpret_cast<uint64_t>(t->v.values_hbm);
+  out->host_values_addr = reinterpret_cast<uint64_t>(t->v.values_host);
   return HKV_OK;
 }
 

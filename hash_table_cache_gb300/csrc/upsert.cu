@@ -1415,6 +1415,7 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
     s.stage_idx = s.map_idx;
     s.stage_inc = s.inc;
   }
+  s.bytes = static_cast<size_t>(p - static_cast<char*>(base));
   return s;
 }
 
