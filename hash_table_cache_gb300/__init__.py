@@ -73,7 +73,8 @@ class OpCounts(ctypes.Structure):
 class Info(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_uint64), ("num_buckets", ctypes.c_uint64),
                 ("hbm_value_rows", ctypes.c_uint64), ("dim", ctypes.c_uint32),
-                ("mode", ctypes.c_uint32), ("device", ctypes.c_int)]
+                ("mode", ctypes.c_uint32), ("device", ctypes.c_int),
+                ("hbm_values_addr", ctypes.c_uint64), ("host_values_addr", ctypes.c_uint64)]
 
 
 _lib = None

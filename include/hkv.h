@@ -14,9 +14,14 @@
  * the table.  An input key in that range is skipped by every call (find
  * reports it not found) and counted; see hkv_get_error_counts.
  *
- * Ranks: an entry's rank is the pair (score, key) compared lexicographically
- * as unsigned integers.  Admission and victim choice use the rank, so equal
- * scores are decided by key.
+ * Ranks: admission and victim choice compare ranks, tuples compared
+ * lexicographically as unsigned integers, so equal scores never leave a
+ * choice open.  Single mode ranks an entry by (score, new, key), where `new`
+ * is 1 for an entry placed by the current call and 0 for one that was
+ * resident before it: an incoming key of equal score outranks an older
+ * entry (HKV Algorithm 2 admits on score >= the bucket minimum), and the key
+ * decides between entries of equal score and age.  Dual mode ranks by
+ * (score, key) (HKV Algorithm 3 admits on score > the minimum).
  *
  * Batches: duplicate keys inside one insert_or_assign or assign batch
  * collapse to their last occurrence.  Inside one insert_or_assign call the
@@ -245,11 +250,16 @@ typedef struct hkv_op_counts {
 hkv_status hkv_get_op_counts(hkv_table* table, hkv_op_counts* out_host);
 hkv_status hkv_reset_op_counts(hkv_table* table);
 
-/* Static facts about a table. */
+/* Static facts about a table.  Value row r (r = bucket * 128 + slot) lives
+ * at device address hbm_values_addr + r * dim * 4 when r < hbm_value_rows,
+ * else at host_values_addr + (r - hbm_value_rows) * dim * 4 (the mapped host
+ * slab of a tiered table; 0 when there is none), so a row address returned
+ * by hkv_find_ptr maps back to its row and bucket. */
 typedef struct hkv_info {
   uint64_t capacity, num_buckets, hbm_value_rows;
   uint32_t dim, mode;
   int device;
+  uint64_t hbm_values_addr, host_values_addr;
 } hkv_info;
 hkv_status hkv_get_info(hkv_table* table, hkv_info* out_host);
 
@@ -275,20 +285,23 @@ hkv_status hkv_set_epoch(hkv_table* table, uint32_t epoch);
  *    plus a(8M) under the LFU policies (2 a(8M) in dual mode), with M the
  *    smallest power of two >= max(64, 2n), B the bucket count and a(x) = x
  *    rounded up to a multiple of 256.  Larger batches return HKV_ERR_INVALID and enqueue
- *    nothing (split them, or use hkv_insert_or_assign).  Single mode takes
- *    up to 2^20 keys per call (2^19 under the LFU policies) for tables of up
- *    to 2^23 buckets.
+ *    nothing (split them, or use hkv_insert_or_assign).  In single mode that
+ *    is up to 2^20 keys per call for tables of at most 2^23 - 256 buckets,
+ *    and up to 2^19 keys under the LFU policies for tables of at most
+ *    12 * 2^20 - 256 buckets; a call of 2^20 + 1 keys (2^19 + 1 under LFU)
+ *    is refused on any table.
  *  - Sharing: every call on every table of a device uses the same array and
  *    clears it before use.  Calls whose kernels overlap on the GPU (on
  *    different streams, from any table) race on it and corrupt each other's
  *    results: keep such calls on one stream, or order them with events.
- *  - Ordering: the call waits for earlier conflicting calls on this table
- *    like hkv_insert_or_assign, but records no event of its own; later calls
- *    on other streams do not wait for it.  Issue them on the same stream or
- *    order them yourself.
+ *  - Ordering on the table: as for hkv_insert_or_assign (an inserter), using
+ *    CUDA events the table created with it, so later calls on other streams,
+ *    hkv_get_op_counts and hkv_destroy wait for this one.
  *  - Set-up: the first call on a device (made with any table of that device)
  *    looks up the array's device address with cudaGetSymbolAddress and keeps
- *    it; make that first call before any stream capture. */
+ *    it for the life of the process; make that first call before any stream
+ *    capture.  cudaDeviceReset on that device destroys its tables and may
+ *    move the array; do not call this function on that device afterwards. */
 #define HKV_NOALLOC_SCRATCH_BYTES (32ull << 20)
 hkv_status hkv_insert_or_assign_noalloc(hkv_table* table, uint64_t n, const uint64_t* keys,
                                         const float* values, const uint64_t* scores, void* stream);
