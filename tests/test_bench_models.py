@@ -1,7 +1,10 @@
 """CPU checks of the benchmark's byte models and bookkeeping: the algorithmic
 bytes per find key against the per-path figures of the HKV find (Algorithm 1:
 key, digest line, expected key confirms, value row in and out, flag, score),
-the insert_or_assign byte count, the random-access floors in limiting cases,
+the insert_or_assign byte counts (slot layout and per-path), the dual-mode
+find bytes, the random-access floors in limiting cases, the hash the bench
+uses to split dual-mode hits (equal to the oracle's buckets), the mapping of
+find* addresses to rows,
 and the rule that a stored ncu traffic figure is reported only while the
 kernel sources it was taken from are unchanged."""
 import hashlib
@@ -43,27 +46,78 @@ def test_upsert_bytes_terms():
 
 
 def test_find_access_floor_limits():
-    rates = {32: 1e9, 128: 1e9}
+    rates = {32: {"plateau": 1e9}, 128: {"plateau": 1e9}}
     huge_bw = 1e30  # streamed bytes cost nothing
     n, nb = 1 << 16, 1 << 10
-    # all misses: half a sector per key plus one line per touched bucket
-    t0 = bench.find_access_floor(n, 32, 0.0, nb, rates, huge_bw)
     lines = nb * (1 - math.exp(-n / nb))
-    assert t0 == pytest.approx(n * 0.5 / 1e9 + lines / 1e9)
+    # all misses: half a sector per key plus one line per touched bucket
+    c0 = bench.find_random_counts(n, 32, 0.0, nb)
+    assert bench.access_floor(c0, 0, rates, huge_bw) == pytest.approx(n * 0.5 / 1e9 + lines / 1e9)
     # all hits at dim 32 (128-byte rows): 1 + 127/256 sectors and a row per key
-    t1 = bench.find_access_floor(n, 32, 1.0, nb, rates, huge_bw)
+    c1 = bench.find_random_counts(n, 32, 1.0, nb)
+    t1 = bench.access_floor(c1, 0, rates, huge_bw)
     assert t1 == pytest.approx(n * (1 + 127 / 256) / 1e9 + n / 1e9 + lines / 1e9)
     # streamed bytes add at the copy bandwidth
-    t2 = bench.find_access_floor(n, 32, 1.0, nb, rates, 1.0)  # 1 GB/s
-    assert t2 - t1 == pytest.approx(n * (8 + 4 * 32 + 8 + 1) / 1e9, rel=1e-6)
+    t2 = bench.access_floor(c1, 1e9, rates, 1.0)  # 1 GB at 1 GB/s
+    assert t2 - t1 == pytest.approx(1.0)
+    # rows wider than 128 bytes are counted at their own granule's rate
+    c3 = bench.find_random_counts(n, 64, 1.0, nb)
+    assert c3[256] == n and c3[32] == pytest.approx(n * (1 + 127 / 256))
 
 
-def test_upsert_access_floor_monotone():
-    rates = {32: 4e10, 128: 2e10}
-    base = bench.upsert_access_floor(1 << 20, 32, 1 << 19, 1 << 15, rates, 6000.0)
-    assert base > 0
-    assert bench.upsert_access_floor(1 << 20, 32, 1 << 20, 1 << 15, rates, 6000.0) > base
-    assert bench.upsert_access_floor(1 << 20, 32, 1 << 19, 1 << 16, rates, 6000.0) > base
+def test_upsert_bytes_paths():
+    d = 4 * 32
+    one = dict(updated=0, admitted=0, evicted=0, rejected=0)
+    # each path alone, one key
+    assert bench.upsert_bytes_paths(dict(one, updated=1), 1, 32) == 164 + 2 * d
+    assert bench.upsert_bytes_paths(dict(one, admitted=1), 1, 32) == 165 + 2 * d
+    assert bench.upsert_bytes_paths(dict(one, admitted=1, evicted=1), 1, 32) == 1189 + 2 * d
+    assert bench.upsert_bytes_paths(dict(one, rejected=1), 1, 32) == 1172
+    # a repeated key of the batch costs its key and row only
+    assert bench.upsert_bytes_paths(dict(one, updated=1), 2, 32) == 164 + 2 * d + 8 + d
+    # dual mode: the second bucket's line, and a second score scan on D2
+    assert bench.upsert_bytes_paths(dict(one, admitted=1), 1, 32, dual=True) == 165 + 2 * d + 132
+    assert bench.upsert_bytes_paths(dict(one, admitted=1, evicted=1), 1, 32,
+                                    dual=True) == 2345 + 2 * d
+    assert bench.upsert_bytes_paths(dict(one, rejected=1), 1, 32, dual=True) == 1172 + 1156
+
+
+def test_find_bytes_dual():
+    hit = bench.find_bytes_per_key(128, 1.0)
+    miss = bench.find_bytes_per_key(128, 0.0)
+    assert bench.find_bytes_dual(128, 1, 0, 0) == pytest.approx(hit)
+    assert bench.find_bytes_dual(128, 0, 1, 0) == pytest.approx(hit + 132)
+    assert bench.find_bytes_dual(128, 0, 0, 1) == pytest.approx(miss + 132)
+
+
+def test_measurement_hash_is_the_documented_hash(oracle_mod):
+    """The bench splits dual-mode hits by bucket with the hash the header
+    documents; it must give the oracle's buckets (both candidates, the b1 =
+    b2 rule included)."""
+    import numpy as np
+    import torch
+    import workloads as wl
+    nb = 1 << 10
+    o = oracle_mod.OracleTable(nb, 4, dual=True)
+    k = wl.unique_keys(5, 200000)
+    kt = torch.from_numpy(wl.as_i64(k))
+    b1 = bench.first_bucket_t(kt, nb).numpy().astype(np.uint64)
+    b2 = bench.second_bucket_t(kt, bench.first_bucket_t(kt, nb), nb).numpy().astype(np.uint64)
+    assert np.array_equal(b1, o.buckets_of(k, 0))
+    assert np.array_equal(b2, o.buckets_of(k, 1))
+    assert (b1 == b2).sum() == 0
+
+
+def test_rows_of_ptrs():
+    import torch
+    info = {"dim": 4, "hbm_value_rows": 256, "hbm_values_addr": 1 << 20,
+            "host_values_addr": 1 << 40}
+    rows = torch.tensor([0, 5, 255, 256, 300, 7])
+    found = torch.tensor([1, 1, 1, 1, 1, 0], dtype=torch.uint8)
+    ptrs = torch.where(rows < 256, (1 << 20) + rows * 16, (1 << 40) + (rows - 256) * 16)
+    got = bench.rows_of_ptrs(ptrs, found, info)
+    assert got[:5].tolist() == [0, 5, 255, 256, 300]
+    assert got[5].item() == 0  # not found
 
 
 def test_ncu_traffic_follows_sources(monkeypatch):
