@@ -68,6 +68,7 @@ struct UpsertExtra {
   float* ev_values = nullptr;
   uint64_t* ev_scores = nullptr;
   unsigned long long* ev_count = nullptr;
+  uint8_t mark_want = 0;  // process only buckets whose mark equals this (0: any mark)
 };
 
 cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n,

@@ -52,6 +52,11 @@ constexpr int kBucketThreads = HKV_BUCKET_THREADS;  // bucket kernel block size
 #ifndef HKV_UPSERT_PREFETCH
 #define HKV_UPSERT_PREFETCH 1
 #endif
+// sparse batches (at most 4 keys per bucket) of plain insert_or_assign take
+// the register-resident bucket pass (upsert_sparse_kernel)
+#ifndef HKV_UPSERT_SPARSE
+#define HKV_UPSERT_SPARSE 1
+#endif
 constexpr uint32_t kHitMark = 0x80000000u;
 
 __device__ __forceinline__ uint32_t map_home(uint64_t key, uint32_t mask) {
@@ -440,7 +445,8 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
 #if HKV_UPSERT_PIPELINE
   // the warp's buckets with keys of the batch (sparse batches mark them)
   auto owned_from = [&](uint64_t x) -> uint64_t {
-    while (x < nb && scr.mark && !scr.mark[x]) x += nwarps;
+    while (x < nb && scr.mark && !(ex.mark_want ? scr.mark[x] == ex.mark_want : scr.mark[x] != 0))
+      x += nwarps;
     return x;
   };
   auto copy_bucket = [&](uint64_t x) {  // lane 0 only
@@ -473,7 +479,9 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
   uint64_t g = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   auto marked = [&](uint64_t g0) -> unsigned {
     const uint64_t x = g0 + lane * nwarps;
-    return __ballot_sync(0xFFFFFFFFu, x < nb && (!scr.mark || scr.mark[x]));
+    return __ballot_sync(0xFFFFFFFFu,
+                         x < nb && (!scr.mark || (ex.mark_want ? scr.mark[x] == ex.mark_want
+                                                               : scr.mark[x] != 0)));
   };
   unsigned todo = marked(g);
   auto next_bucket = [&]() -> uint64_t {
@@ -978,6 +986,325 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
 }
 
 // ---------------------------------------------------------------------------
+// Sparse-batch bucket pass (single mode, plain insert_or_assign, batches of
+// at most four keys per table bucket on average: large tables fed skewed or
+// modest batches).  Most touched buckets then hold one or two of the batch's
+// keys, and a warp per bucket spends about a thousand instructions on set-up
+// and warp-wide steps whatever the bucket receives.  Here an 8-lane tile
+// owns a bucket (four buckets per warp), and it handles the cases sparse
+// batches consist of:
+//   * every key of the bucket's stage run is looked up through the digest
+//     line (HKV Algorithm 1) and the (key, score) pairs of its candidates;
+//     resident keys get their new score and row (Algorithm 2, found branch);
+//   * absent keys that fit in the bucket's free slots take them in slot
+//     order (the lane order of the keys), without reading any score;
+//   * a full bucket receiving one or two absent keys (and no resident one):
+//     the tile streams the bucket's 128 pairs once, each lane keeping its two
+//     lowest (score, key), merges them across the tile, and removes the
+//     lowest one or two ranks of those residents and the incoming keys
+//     (rank (score, new, key): an incoming key outranks a resident of equal
+//     score); incoming keys left take the removed residents' slots.
+// Any other bucket (a stage run longer than 8 positions, more than four
+// keys, free slots too few for its absent keys but not none, more than two
+// evictions, or resident keys beside evictions) is left untouched and marked
+// for the general bucket kernel, which a second launch runs on those
+// buckets only.  The results equal the general kernel's: every bucket ends
+// with the 128 highest ranks of its residents (after their updates) and its
+// absent keys.
+// ---------------------------------------------------------------------------
+#ifndef HKV_TILE_MIN_BLOCKS
+#define HKV_TILE_MIN_BLOCKS 4
+#endif
+constexpr uint8_t kMarkDeferred = 2;
+constexpr int kTileMaxEntries = 4;
+
+__device__ __forceinline__ bool sk_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
+  return s1 < s2 || (s1 == s2 && k1 < k2);
+}
+
+// Minimum of (score, key) over the 8 lanes of a tile, with its slot.
+__device__ __forceinline__ void tile_min_sk(uint64_t& s, uint64_t& k, uint32_t& slot,
+                                            unsigned tmask) {
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    const uint64_t s2 = __shfl_xor_sync(tmask, s, o);
+    const uint64_t k2 = __shfl_xor_sync(tmask, k, o);
+    const uint32_t l2 = __shfl_xor_sync(tmask, slot, o);
+    if (sk_less(s2, k2, s, k)) {
+      s = s2;
+      k = k2;
+      slot = l2;
+    }
+  }
+}
+
+template <bool kLfu>
+__global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_kernel(
+    TableView t, UpsertScratch scr, const float* values_in, ScoreRule rule, bool vec) {
+  // per tile: the value rows to copy for its bucket (slot, batch index)
+  __shared__ uint8_t rslot_sh[kThreads / 8][2 * kTileMaxEntries];
+  __shared__ uint32_t ridx_sh[kThreads / 8][2 * kTileMaxEntries];
+  pdl_wait();
+  pdl_trigger();
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const unsigned lane = lane_id();
+  const unsigned sub = lane & 7u;
+  const unsigned tb = lane & 24u;
+  const unsigned tmask = 0xFFu << tb;
+  uint8_t* rslot = rslot_sh[threadIdx.x >> 3];
+  uint32_t* ridx = ridx_sh[threadIdx.x >> 3];
+  auto score_of = [&](uint32_t e, uint64_t inc, bool resident, uint64_t old) -> uint64_t {
+    if (kLfu) return policy_score(rule, e, inc, resident, old);
+    return rule.in ? rule.in[e] : rule.clock;
+  };
+  const uint64_t T = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 3;
+  const uint64_t tile = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+  const uint64_t nb = t.num_buckets;
+  const uint64_t S = scr.map_size, smask = S - 1;
+  uint32_t n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0;  // lane sub == 0 of each tile
+
+  // the tile's buckets tile, tile + T, ..., eight candidates per mark load
+  for (uint64_t g0 = tile; g0 < nb; g0 += 8 * T) {
+    const uint64_t x = g0 + sub * T;
+    unsigned todo = (__ballot_sync(tmask, x < nb && scr.mark[x] == 1) >> tb) & 0xFFu;
+    while (todo) {
+      const uint64_t b = g0 + (__ffs(todo) - 1) * T;
+      todo &= todo - 1;
+      const uint64_t row0 = b * kSlots;
+      // ---- the bucket's stage run: 8 positions from its area's start
+      const uint64_t lo = area_start(b, S, nb, scr.area_shift);
+      const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
+      const uint64_t jpos = lo + sub;
+      const uint64_t key = scr.stage_keys[jpos & smask];
+      const uint32_t raw = scr.stage_idx[jpos & smask];
+      const uint64_t inc = kLfu ? scr.stage_inc[jpos & smask] : 0ull;
+      const uint32_t e = (raw & ~kHitMark) - 1;
+      const bool empty = key == kEmptyKey;
+      const unsigned stopm = (__ballot_sync(tmask, empty && jpos >= a_end) >> tb) & 0xFFu;
+      const bool mine = stopm && !empty && sub < static_cast<unsigned>(__ffs(stopm) - 1) &&
+                        bucket_of_hash(t, hash64(key)) == b;
+      const unsigned em = (__ballot_sync(tmask, mine) >> tb) & 0xFFu;
+      if (!stopm || __popc(em) > kTileMaxEntries) {  // long run or many keys
+        if (sub == 0) scr.mark[b] = kMarkDeferred;
+        continue;
+      }
+      // ---- look every key up (this lane: digest bytes of slots 16 sub ..)
+      const uint4 dg = *reinterpret_cast<const uint4*>(t.digests + row0 + sub * 16);
+      int my_hit = -1;  // in the key's lane: its slot when resident
+      uint64_t my_old = 0;
+      for (unsigned m = em; m; m &= m - 1) {
+        const unsigned src = tb + __ffs(m) - 1;
+        const uint64_t ke = __shfl_sync(tmask, key, src);
+        const uint32_t pat = digest_of_hash(hash64(ke)) * 0x01010101u;
+        uint32_t cm = byte_match4(dg.x, pat) | (byte_match4(dg.y, pat) << 4) |
+                      (byte_match4(dg.z, pat) << 8) | (byte_match4(dg.w, pat) << 12);
+        int hs = -1;
+        uint64_t old = 0;
+        while (cm) {
+          const int c = __ffs(cm) - 1;
+          cm &= cm - 1;
+          const ulonglong2 p = *reinterpret_cast<const ulonglong2*>(key_at(t, row0 + sub * 16 + c));
+          if (p.x == ke) {
+            hs = static_cast<int>(sub * 16 + c);
+            old = p.y;
+            break;
+          }
+        }
+        const unsigned hb = (__ballot_sync(tmask, hs >= 0) >> tb) & 0xFFu;
+        const unsigned from = hb ? tb + __ffs(hb) - 1 : src;
+        const int s2 = __shfl_sync(tmask, hs, from);
+        const uint64_t o2 = __shfl_sync(tmask, old, from);
+        if (lane == src && hb) {
+          my_hit = s2;
+          my_old = o2;
+        }
+      }
+      const unsigned hm = (__ballot_sync(tmask, my_hit >= 0) >> tb) & 0xFFu;
+      const unsigned am = em & ~hm;
+      const uint32_t A = __popc(am);
+      // free slots: zero digest bytes (bit j = slot 16 sub + j)
+      const uint32_t fm = byte_eq_mask4(dg.x, 0u) | (byte_eq_mask4(dg.y, 0u) << 4) |
+                          (byte_eq_mask4(dg.z, 0u) << 8) | (byte_eq_mask4(dg.w, 0u) << 12);
+      const uint32_t nf = __popc(fm);
+      uint32_t pre = nf;  // inclusive prefix over the tile's lanes, then exclusive
+#pragma unroll
+      for (int d = 1; d < 8; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(tmask, pre, d, 8);
+        if (sub >= static_cast<unsigned>(d)) pre += y;
+      }
+      const uint32_t F = __shfl_sync(tmask, pre, tb + 7);
+      pre -= nf;
+      const bool evict = A > F;
+      if (evict && (F != 0 || A > 2 || hm != 0)) {  // a case for the general kernel
+        if (sub == 0) scr.mark[b] = kMarkDeferred;
+        continue;
+      }
+      // ---- apply: resident keys (new score now, row below)
+      uint32_t nrow = 0;
+      for (unsigned m = hm; m; m &= m - 1) {
+        const unsigned src = tb + __ffs(m) - 1;
+        const int hs = __shfl_sync(tmask, my_hit, src);
+        const uint32_t ee = __shfl_sync(tmask, e, src);
+        const uint64_t ei = kLfu ? __shfl_sync(tmask, inc, src) : 0ull;
+        const uint64_t old = __shfl_sync(tmask, my_old, src);
+        if (sub == 0) {
+          *score_at(t, row0 + hs) = score_of(ee, ei, true, old);
+          rslot[nrow] = static_cast<uint8_t>(hs);
+          ridx[nrow] = ee;
+        }
+        ++nrow;
+      }
+      if (sub == 0) n_upd += __popc(hm);
+      if (A && !evict) {
+        // free slots in slot order to the absent keys in lane order
+        uint32_t r = 0;
+        for (unsigned m = am; m; m &= m - 1, ++r) {
+          const unsigned src = tb + __ffs(m) - 1;
+          const uint64_t ke = __shfl_sync(tmask, key, src);
+          const uint32_t ee = __shfl_sync(tmask, e, src);
+          const uint64_t ei = kLfu ? __shfl_sync(tmask, inc, src) : 0ull;
+          if (pre <= r && r < pre + nf) {
+            const uint32_t slot = sub * 16 + (__fns(fm, 0, static_cast<int>(r - pre + 1)));
+            *reinterpret_cast<ulonglong2*>(key_at(t, row0 + slot)) =
+                make_ulonglong2(ke, score_of(ee, ei, false, 0ull));
+            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(ke)));
+            rslot[nrow] = static_cast<uint8_t>(slot);
+            ridx[nrow] = ee;
+          }
+          ++nrow;
+        }
+        if (sub == 0) n_adm += A;
+      } else if (evict) {
+        // full bucket, one or two incoming keys: the lane's two lowest
+        // (score, key) over its slots 8 i + sub
+        uint64_t s1 = ~0ull, k1 = ~0ull, s2 = ~0ull, k2 = ~0ull;
+        uint32_t l1 = kNone, l2 = kNone;
+#pragma unroll
+        for (int g = 0; g < 16; g += 4) {
+          ulonglong2 p[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            p[i] = *reinterpret_cast<const ulonglong2*>(key_at(t, row0 + 8 * (g + i) + sub));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t slot = 8 * (g + i) + sub;
+            if (sk_less(p[i].y, p[i].x, s2, k2)) {
+              if (sk_less(p[i].y, p[i].x, s1, k1)) {
+                s2 = s1;
+                k2 = k1;
+                l2 = l1;
+                s1 = p[i].y;
+                k1 = p[i].x;
+                l1 = slot;
+              } else {
+                s2 = p[i].y;
+                k2 = p[i].x;
+                l2 = slot;
+              }
+            }
+          }
+        }
+        // the bucket's lowest resident R0, and its second lowest R1 for two keys
+        uint64_t rs0 = s1, rk0 = k1, rs1 = ~0ull, rk1 = ~0ull;
+        uint32_t rl0 = l1, rl1 = kNone;
+        tile_min_sk(rs0, rk0, rl0, tmask);
+        if (A == 2) {
+          if (l1 == rl0) {
+            s1 = s2;
+            k1 = k2;
+            l1 = l2;
+          }
+          rs1 = s1;
+          rk1 = k1;
+          rl1 = l1;
+          tile_min_sk(rs1, rk1, rl1, tmask);
+        }
+        // the incoming keys P0 (and P1), in lane order
+        const unsigned src0 = tb + __ffs(am) - 1;
+        const unsigned src1 = A == 2 ? tb + __ffs(am & (am - 1)) - 1 : src0;
+        const uint64_t pk0 = __shfl_sync(tmask, key, src0), pk1 = __shfl_sync(tmask, key, src1);
+        const uint32_t pe0 = __shfl_sync(tmask, e, src0), pe1 = __shfl_sync(tmask, e, src1);
+        const uint64_t pi0 = kLfu ? __shfl_sync(tmask, inc, src0) : 0ull;
+        const uint64_t pi1 = kLfu ? __shfl_sync(tmask, inc, src1) : 0ull;
+        const uint64_t ps0 = score_of(pe0, pi0, false, 0ull), ps1 = score_of(pe1, pi1, false, 0ull);
+        // the A lowest ranks of {R0, .., P0, ..} go (residents rank (score, 0,
+        // key), incoming keys (score, 1, key)); R0 ranks below R1
+        bool gr0, gr1 = false, gp0, gp1 = false;
+        if (A == 1) {
+          gp0 = rank3_less(ps0, 1u, pk0, rs0, 0u, rk0);
+          gr0 = !gp0;
+        } else {
+          const uint32_t br0 = (rank3_less(ps0, 1u, pk0, rs0, 0u, rk0) ? 1u : 0u) +
+                               (rank3_less(ps1, 1u, pk1, rs0, 0u, rk0) ? 1u : 0u);
+          const uint32_t br1 = 1u + (rank3_less(ps0, 1u, pk0, rs1, 0u, rk1) ? 1u : 0u) +
+                               (rank3_less(ps1, 1u, pk1, rs1, 0u, rk1) ? 1u : 0u);
+          const bool p1lt0 = rank3_less(ps1, 1u, pk1, ps0, 1u, pk0);
+          const uint32_t bp0 = (rank3_less(rs0, 0u, rk0, ps0, 1u, pk0) ? 1u : 0u) +
+                               (rank3_less(rs1, 0u, rk1, ps0, 1u, pk0) ? 1u : 0u) + (p1lt0 ? 1u : 0u);
+          const uint32_t bp1 = (rank3_less(rs0, 0u, rk0, ps1, 1u, pk1) ? 1u : 0u) +
+                               (rank3_less(rs1, 0u, rk1, ps1, 1u, pk1) ? 1u : 0u) + (p1lt0 ? 0u : 1u);
+          gr0 = br0 < 2;
+          gr1 = br1 < 2;
+          gp0 = bp0 < 2;
+          gp1 = bp1 < 2;
+        }
+        // surviving incoming keys take the removed residents' slots: both, or
+        // the one survivor takes R0's
+        const uint32_t ev = (gr0 ? 1u : 0u) + (gr1 ? 1u : 0u);
+        const uint32_t rj = (gp0 ? 1u : 0u) + (gp1 ? 1u : 0u);
+        auto put = [&](uint32_t slot, uint64_t k, uint64_t sc, uint32_t ee) {
+          if (sub == 0) {
+            *reinterpret_cast<ulonglong2*>(key_at(t, row0 + slot)) = make_ulonglong2(k, sc);
+            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(k)));
+            rslot[nrow] = static_cast<uint8_t>(slot);
+            ridx[nrow] = ee;
+          }
+          ++nrow;
+        };
+        if (ev == 2) {
+          put(rl0, pk0, ps0, pe0);
+          put(rl1, pk1, ps1, pe1);
+        } else if (ev == 1) {
+          if (!gp0) put(rl0, pk0, ps0, pe0);
+          else put(rl0, pk1, ps1, pe1);
+        }
+        if (sub == 0) {
+          n_adm += ev;
+          n_evi += ev;
+          n_rej += rj;
+        }
+      }
+      // ---- the changed slots' value rows, four in flight
+      __syncwarp(tmask);
+      float* const rows = row_ptr(t, row0);
+      for (uint32_t i = 0; i < nrow; i += 4) {
+        float* dst[4];
+        const float* src[4];
+        bool ok[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          ok[r] = i + r < nrow;
+          dst[r] = rows + (ok[r] ? rslot[i + r] : 0) * t.dim;
+          src[r] = values_in + static_cast<uint64_t>(ok[r] ? ridx[i + r] : 0) * t.dim;
+        }
+        tile_copy_rows<4>(dst, src, ok, t.dim, sub, vec);
+      }
+      __syncwarp(tmask);  // the row list is read before the next bucket writes it
+    }
+  }
+  const uint32_t u = __reduce_add_sync(kFull, n_upd), ad = __reduce_add_sync(kFull, n_adm);
+  const uint32_t ev = __reduce_add_sync(kFull, n_evi), rj = __reduce_add_sync(kFull, n_rej);
+  if (lane == 0) {
+    using ull = unsigned long long;
+    if (u) atomicAdd(&t.stats->updated, static_cast<ull>(u));
+    if (ad) atomicAdd(&t.stats->admitted, static_cast<ull>(ad));
+    if (ev) atomicAdd(&t.stats->evicted, static_cast<ull>(ev));
+    if (rj) atomicAdd(&t.stats->rejected, static_cast<ull>(rj));
+    if (ad != ev) atomicAdd(&t.stats->size, static_cast<ull>(ad) - static_cast<ull>(ev));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Dual mode (Algorithm 3), as routing plus bucket ownership.
 //
 // Algorithm 3 sends an absent key to one of its two buckets: the less
@@ -1357,6 +1684,12 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 namespace {
+// A batch of at most four keys per table bucket on average: the stage marks
+// the buckets it touches (the bucket passes visit only those), collapses
+// repeated keys inside each warp, and plain insert_or_assign takes the
+// register-resident bucket pass.
+bool sparse_batch(uint64_t n, uint64_t num_buckets) { return n <= 4 * num_buckets; }
+
 #ifndef HKV_STAGE_FACTOR
 #define HKV_STAGE_FACTOR 2
 #endif
@@ -1399,7 +1732,7 @@ UpsertScratch carve_upsert_scratch(void* base, uint64_t n, uint64_t num_buckets,
   s.cursor = reinterpret_cast<uint32_t*>(take(64));
   if (kind == ScratchKind::kSingleUpsert) {
     s.mark = reinterpret_cast<uint8_t*>(take(num_buckets));
-    if (n >= 2 * num_buckets) s.mark = nullptr;  // dense batch: no marks
+    if (!sparse_batch(n, num_buckets)) s.mark = nullptr;  // dense batch: no marks
   }
   if (lfu) s.inc = reinterpret_cast<uint64_t*>(take(m * 8));
   if (kind == ScratchKind::kDualUpsert) {
@@ -1492,6 +1825,30 @@ cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const
                                                            ex);
 }
 
+// The sparse-batch pass (single mode, plain insert_or_assign): the tile
+// kernel, then the general kernel on the buckets it deferred.
+cudaError_t launch_sparse_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
+                               const float* values, const ScoreRule& rule, bool vec,
+                               cudaStream_t st) {
+  uint64_t blocks = (t.num_buckets * 8 + kThreads - 1) / kThreads;
+  const uint64_t cap = static_cast<uint64_t>(sm_count()) * HKV_TILE_MIN_BLOCKS;
+  const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
+  ScoreRule r = rule;
+  if (!rule.lfu()) {
+    if (rule.policy != kCustomized) r.in = nullptr;
+    if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
+    r.policy = kCustomized;
+  }
+  cudaError_t e =
+      rule.lfu()
+          ? launch_chained(upsert_tile_kernel<true>, grid, kThreads, 0, st, t, s, values, r, vec)
+          : launch_chained(upsert_tile_kernel<false>, grid, kThreads, 0, st, t, s, values, r, vec);
+  if (e != cudaSuccess) return e;
+  UpsertExtra deferred;
+  deferred.mark_want = kMarkDeferred;
+  return launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, deferred);
+}
+
 }  // namespace
 
 cudaError_t clear_upsert_scratch(const UpsertScratch& s, uint64_t num_buckets, ScratchKind kind,
@@ -1511,9 +1868,12 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
   cudaError_t e = cudaSuccess;
   if (!t.dual) {
     const unsigned sg = grid_for((n + kStageKeysPerThread - 1) / kStageKeysPerThread);
-    const bool sparse = n <= 4 * t.num_buckets;  // a few keys per bucket
+    const bool sparse = sparse_batch(n, t.num_buckets);
     e = sparse ? launch_chained(stage_kernel<true>, sg, kThreads, 0, st, t, s, n, keys, inc_in)
                : launch_chained(stage_kernel<false>, sg, kThreads, 0, st, t, s, n, keys, inc_in);
+    const bool plain = ex.update_resident && !ex.ev_keys;
+    if (e == cudaSuccess && sparse && plain && HKV_UPSERT_SPARSE)
+      return launch_sparse_pass(t, s, keys, values, rule, vec, st);
     if (e == cudaSuccess) e = launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, ex);
     return e;
   }

@@ -92,6 +92,51 @@ def test_random_ops_bit_exact(hkv, oracle_mod, num_buckets, dim, seed):
     assert errs["timeouts"] == 0
 
 
+@pytest.mark.parametrize("policy", ["custom", "lfu"])
+@pytest.mark.parametrize("num_buckets,dim", [(64, 8), (300, 4), (1024, 16)])
+def test_sparse_batches_bit_exact(hkv, oracle_mod, policy, num_buckets, dim):
+    """Batches of at most four keys per bucket (the sparse path: one tile per
+    touched bucket, the general kernel for the buckets it defers), on tables
+    from empty to full: free-slot placement, one or two evictions per full
+    bucket, resident keys beside absent ones, ties of score (small score
+    range, or the step counter), repeated keys (last occurrence wins) and
+    reserved keys; the whole table, the counts and a find compared with the
+    oracle after every call."""
+    rng = np.random.default_rng(num_buckets + dim)
+    cap = num_buckets * 128
+    mode = hkv.HKV_POLICY_LFU if policy == "lfu" else 0
+    t = hkv.HashTable(cap, dim, mode=mode)
+    o = oracle_mod.OracleTable(num_buckets, dim,
+                               policy=oracle_mod.POLICY_LFU if policy == "lfu" else 0)
+    universe = wl.unique_keys(num_buckets + 991, 3 * cap)
+    for step in range(40):
+        n = int(rng.integers(1, 4 * num_buckets + 1))
+        if step < 8:  # fill with fresh keys first, then mixes
+            keys = universe[step * (cap // 4):step * (cap // 4) + n]
+        else:
+            keys = universe[rng.integers(0, universe.size, n)]
+        if rng.random() < 0.3:
+            keys[rng.integers(0, n)] = hkv.RESERVED_KEY_LO + int(rng.integers(0, 16))
+        if rng.random() < 0.3:
+            keys[rng.integers(0, n, max(1, n // 8))] = keys[0]  # repeats
+        vals = rng.standard_normal((n, dim)).astype(np.float32)
+        r = rng.random()
+        scores = None if r < 0.3 else rng.integers(0, 4 if r < 0.6 else 1 << 40, n).astype(np.uint64)
+        t.reset_op_counts()
+        t.insert_or_assign(dkeys(keys), dvals(vals), None if scores is None else dkeys(scores))
+        oc = o.insert_or_assign(keys, vals, scores)
+        gc = t.op_counts()
+        for f in ("updated", "admitted", "evicted", "rejected"):
+            assert gc[f] == oc[f], (step, f, gc, oc)
+        assert_same_state(t, o)
+        assert t.size() == o.size()
+        if step % 5 == 4:
+            q = np.concatenate([universe[rng.integers(0, universe.size, 500)],
+                                wl.unique_keys(num_buckets + 5, 100, step * 100)])
+            find_compare(t, o, q)
+    t.close()
+
+
 def test_c2_lambda_sweep(hkv, oracle_mod):
     """Capacity 2^22, dim 32: fill with unique keys in batches of 2^16 scored by
     the step counter; at load factor 0.50, 0.75, 0.90 and 1.00 compare a find
