@@ -991,47 +991,45 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
 // modest batches).  Most touched buckets then hold one or two of the batch's
 // keys, and a warp per bucket spends about a thousand instructions on set-up
 // and warp-wide steps whatever the bucket receives.  Here an 8-lane tile
-// owns a bucket (four buckets per warp), and it handles the cases sparse
-// batches consist of:
-//   * every key of the bucket's stage run is looked up through the digest
-//     line (HKV Algorithm 1) and the (key, score) pairs of its candidates;
-//     resident keys get their new score and row (Algorithm 2, found branch);
-//   * absent keys that fit in the bucket's free slots take them in slot
-//     order (the lane order of the keys), without reading any score;
-//   * a full bucket receiving one or two absent keys (and no resident one):
-//     the tile streams the bucket's 128 pairs once, each lane keeping its two
-//     lowest (score, key), merges them across the tile, and removes the
-//     lowest one or two ranks of those residents and the incoming keys
-//     (rank (score, new, key): an incoming key outranks a resident of equal
-//     score); incoming keys left take the removed residents' slots.
-// Any other bucket (a stage run longer than 8 positions, more than four
-// keys, free slots too few for its absent keys but not none, more than two
-// evictions, or resident keys beside evictions) is left untouched and marked
-// for the general bucket kernel, which a second launch runs on those
-// buckets only.  The results equal the general kernel's: every bucket ends
-// with the 128 highest ranks of its residents (after their updates) and its
-// absent keys.
+// owns a bucket (four buckets per warp):
+//   1. it reads the first 16 positions of the bucket's stage run and lists
+//      the bucket's keys (at most 8) in stage order;
+//   2. every key is looked up through the digest line (HKV Algorithm 1) and
+//      the (key, score) pairs of its candidate slots; a resident key gets its
+//      new score (Algorithm 2, found branch), all before any placement;
+//   3. the absent keys take the free slots (zero digest bytes) in slot order;
+//   4. for the E absent keys left the tile removes, E times, the lowest rank
+//      (score, new, key) among the bucket's slots and those keys: one pass
+//      over the bucket's 128 pairs (16 per lane) and a tile arg-min per
+//      removal (an incoming key outranks a resident of equal score); the
+//      keys still pending take the removed slots;
+//   5. key / score pairs and digest bytes are written as decided, and the
+//      value rows of the keys that ended resident are copied, four in flight.
+// A bucket whose run does not end within 16 positions, or that has more than
+// 8 keys, is left untouched and marked for the general bucket kernel, which a
+// second launch runs on those buckets only.  The results equal the general
+// kernel's: each bucket ends with the 128 highest ranks of its residents
+// (after their updates) and its absent keys.
 // ---------------------------------------------------------------------------
 #ifndef HKV_TILE_MIN_BLOCKS
 #define HKV_TILE_MIN_BLOCKS 4
 #endif
 constexpr uint8_t kMarkDeferred = 2;
-constexpr int kTileMaxEntries = 4;
+constexpr int kTileRun = 16;       // stage positions a tile reads, two per lane
+constexpr int kTileMaxEntries = 8;  // keys per bucket the tile path takes
 
-__device__ __forceinline__ bool sk_less(uint64_t s1, uint64_t k1, uint64_t s2, uint64_t k2) {
-  return s1 < s2 || (s1 == s2 && k1 < k2);
-}
-
-// Minimum of (score, key) over the 8 lanes of a tile, with its slot.
-__device__ __forceinline__ void tile_min_sk(uint64_t& s, uint64_t& k, uint32_t& slot,
-                                            unsigned tmask) {
+// Lowest rank (score, new, key) over the 8 lanes of a tile, with its slot.
+__device__ __forceinline__ void tile_min_rank(uint64_t& s, uint32_t& nw, uint64_t& k,
+                                              uint32_t& slot, unsigned tmask) {
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) {
     const uint64_t s2 = __shfl_xor_sync(tmask, s, o);
+    const uint32_t n2 = __shfl_xor_sync(tmask, nw, o);
     const uint64_t k2 = __shfl_xor_sync(tmask, k, o);
     const uint32_t l2 = __shfl_xor_sync(tmask, slot, o);
-    if (sk_less(s2, k2, s, k)) {
+    if (rank3_less(s2, n2, k2, s, nw, k)) {
       s = s2;
+      nw = n2;
       k = k2;
       slot = l2;
     }
@@ -1041,18 +1039,29 @@ __device__ __forceinline__ void tile_min_sk(uint64_t& s, uint64_t& k, uint32_t& 
 template <bool kLfu>
 __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_kernel(
     TableView t, UpsertScratch scr, const float* values_in, ScoreRule rule, bool vec) {
-  // per tile: the value rows to copy for its bucket (slot, batch index)
-  __shared__ uint8_t rslot_sh[kThreads / 8][2 * kTileMaxEntries];
-  __shared__ uint32_t ridx_sh[kThreads / 8][2 * kTileMaxEntries];
+  // per tile, its bucket's keys in stage order: key, batch index, increment,
+  // score (absent keys), the slot a resident key holds or an absent key
+  // ends in (-1: none), and a resident key's old score
+  constexpr int kTiles = kThreads / 8;
+  __shared__ uint64_t ekey_sh[kTiles][kTileMaxEntries];
+  __shared__ uint64_t einc_sh[kTiles][kTileMaxEntries];
+  __shared__ uint64_t escore_sh[kTiles][kTileMaxEntries];
+  __shared__ uint32_t eidx_sh[kTiles][kTileMaxEntries];
+  __shared__ int32_t eslot_sh[kTiles][kTileMaxEntries];
+  __shared__ uint8_t xslot_sh[kTiles][kTileMaxEntries];  // slots removed, in order
   pdl_wait();
   pdl_trigger();
-  constexpr unsigned kFull = 0xFFFFFFFFu;
   const unsigned lane = lane_id();
   const unsigned sub = lane & 7u;
   const unsigned tb = lane & 24u;
   const unsigned tmask = 0xFFu << tb;
-  uint8_t* rslot = rslot_sh[threadIdx.x >> 3];
-  uint32_t* ridx = ridx_sh[threadIdx.x >> 3];
+  const int tw = threadIdx.x >> 3;
+  uint64_t* ekey = ekey_sh[tw];
+  uint64_t* einc = einc_sh[tw];
+  uint64_t* escore = escore_sh[tw];
+  uint32_t* eidx = eidx_sh[tw];
+  int32_t* eslot = eslot_sh[tw];
+  uint8_t* xslot = xslot_sh[tw];
   auto score_of = [&](uint32_t e, uint64_t inc, bool resident, uint64_t old) -> uint64_t {
     if (kLfu) return policy_score(rule, e, inc, resident, old);
     return rule.in ? rule.in[e] : rule.clock;
@@ -1071,30 +1080,49 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       const uint64_t b = g0 + (__ffs(todo) - 1) * T;
       todo &= todo - 1;
       const uint64_t row0 = b * kSlots;
-      // ---- the bucket's stage run: 8 positions from its area's start
+      // ---- 1. the bucket's keys: stage positions lo + sub and lo + 8 + sub
       const uint64_t lo = area_start(b, S, nb, scr.area_shift);
       const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
-      const uint64_t jpos = lo + sub;
-      const uint64_t key = scr.stage_keys[jpos & smask];
-      const uint32_t raw = scr.stage_idx[jpos & smask];
-      const uint64_t inc = kLfu ? scr.stage_inc[jpos & smask] : 0ull;
-      const uint32_t e = (raw & ~kHitMark) - 1;
-      const bool empty = key == kEmptyKey;
-      const unsigned stopm = (__ballot_sync(tmask, empty && jpos >= a_end) >> tb) & 0xFFu;
-      const bool mine = stopm && !empty && sub < static_cast<unsigned>(__ffs(stopm) - 1) &&
-                        bucket_of_hash(t, hash64(key)) == b;
-      const unsigned em = (__ballot_sync(tmask, mine) >> tb) & 0xFFu;
-      if (!stopm || __popc(em) > kTileMaxEntries) {  // long run or many keys
+      uint64_t key[2], inc[2];
+      uint32_t raw[2];
+      unsigned stop = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t j = lo + 8 * h + sub;
+        key[h] = scr.stage_keys[j & smask];
+        raw[h] = scr.stage_idx[j & smask];
+        inc[h] = kLfu ? scr.stage_inc[j & smask] : 0ull;
+        stop |= ((__ballot_sync(tmask, key[h] == kEmptyKey && j >= a_end) >> tb) & 0xFFu) << (8 * h);
+      }
+      const int end = stop ? __ffs(stop) - 1 : kTileRun;  // first position past the run
+      unsigned em = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool mine = key[h] != kEmptyKey && static_cast<int>(8 * h + sub) < end &&
+                          bucket_of_hash(t, hash64(key[h])) == b;
+        em |= ((__ballot_sync(tmask, mine) >> tb) & 0xFFu) << (8 * h);
+      }
+      const int ne = __popc(em);
+      if (!stop || ne > kTileMaxEntries) {  // a long run or many keys: general kernel
         if (sub == 0) scr.mark[b] = kMarkDeferred;
         continue;
       }
-      // ---- look every key up (this lane: digest bytes of slots 16 sub ..)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const unsigned pos = 8 * h + sub;
+        if ((em >> pos) & 1u) {
+          const int i = __popc(em & ((1u << pos) - 1u));
+          ekey[i] = key[h];
+          eidx[i] = (raw[h] & ~kHitMark) - 1;
+          einc[i] = inc[h];
+        }
+      }
+      __syncwarp(tmask);
+      // ---- 2. look every key up (this lane: digest bytes of slots 16 sub ..)
       const uint4 dg = *reinterpret_cast<const uint4*>(t.digests + row0 + sub * 16);
-      int my_hit = -1;  // in the key's lane: its slot when resident
-      uint64_t my_old = 0;
-      for (unsigned m = em; m; m &= m - 1) {
-        const unsigned src = tb + __ffs(m) - 1;
-        const uint64_t ke = __shfl_sync(tmask, key, src);
+      unsigned hm = 0;  // entries resident
+      for (int i = 0; i < ne; ++i) {
+        const uint64_t ke = ekey[i];
         const uint32_t pat = digest_of_hash(hash64(ke)) * 0x01010101u;
         uint32_t cm = byte_match4(dg.x, pat) | (byte_match4(dg.y, pat) << 4) |
                       (byte_match4(dg.z, pat) << 8) | (byte_match4(dg.w, pat) << 12);
@@ -1111,18 +1139,22 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
           }
         }
         const unsigned hb = (__ballot_sync(tmask, hs >= 0) >> tb) & 0xFFu;
-        const unsigned from = hb ? tb + __ffs(hb) - 1 : src;
-        const int s2 = __shfl_sync(tmask, hs, from);
-        const uint64_t o2 = __shfl_sync(tmask, old, from);
-        if (lane == src && hb) {
-          my_hit = s2;
-          my_old = o2;
+        if (hb) {
+          hm |= 1u << i;
+          if (sub == static_cast<unsigned>(__ffs(hb) - 1)) {  // the lane that found it
+            eslot[i] = hs;
+            *score_at(t, row0 + hs) = score_of(eidx[i], einc[i], true, old);
+          }
+        } else if (sub == 0) {
+          eslot[i] = -1;
+          escore[i] = score_of(eidx[i], einc[i], false, 0ull);
         }
       }
-      const unsigned hm = (__ballot_sync(tmask, my_hit >= 0) >> tb) & 0xFFu;
-      const unsigned am = em & ~hm;
-      const uint32_t A = __popc(am);
-      // free slots: zero digest bytes (bit j = slot 16 sub + j)
+      const uint32_t nh = __popc(hm);
+      const uint32_t A = ne - nh;
+      if (sub == 0) n_upd += nh;
+      // ---- 3. free slots (zero digest bytes; bit j = slot 16 sub + j) to the
+      // absent keys in stage order, in slot order
       const uint32_t fm = byte_eq_mask4(dg.x, 0u) | (byte_eq_mask4(dg.y, 0u) << 4) |
                           (byte_eq_mask4(dg.z, 0u) << 8) | (byte_eq_mask4(dg.w, 0u) << 12);
       const uint32_t nf = __popc(fm);
@@ -1134,164 +1166,135 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       }
       const uint32_t F = __shfl_sync(tmask, pre, tb + 7);
       pre -= nf;
-      const bool evict = A > F;
-      if (evict && (F != 0 || A > 2 || hm != 0)) {  // a case for the general kernel
-        if (sub == 0) scr.mark[b] = kMarkDeferred;
-        continue;
-      }
-      // ---- apply: resident keys (new score now, row below)
-      uint32_t nrow = 0;
-      for (unsigned m = hm; m; m &= m - 1) {
-        const unsigned src = tb + __ffs(m) - 1;
-        const int hs = __shfl_sync(tmask, my_hit, src);
-        const uint32_t ee = __shfl_sync(tmask, e, src);
-        const uint64_t ei = kLfu ? __shfl_sync(tmask, inc, src) : 0ull;
-        const uint64_t old = __shfl_sync(tmask, my_old, src);
-        if (sub == 0) {
-          *score_at(t, row0 + hs) = score_of(ee, ei, true, old);
-          rslot[nrow] = static_cast<uint8_t>(hs);
-          ridx[nrow] = ee;
-        }
-        ++nrow;
-      }
-      if (sub == 0) n_upd += __popc(hm);
-      if (A && !evict) {
-        // free slots in slot order to the absent keys in lane order
+      __syncwarp(tmask);  // escore / eslot written above
+      const unsigned amask = ((1u << ne) - 1u) & ~hm;  // absent entries
+      unsigned pend = amask;                           // absent entries not placed yet
+      {
         uint32_t r = 0;
-        for (unsigned m = am; m; m &= m - 1, ++r) {
-          const unsigned src = tb + __ffs(m) - 1;
-          const uint64_t ke = __shfl_sync(tmask, key, src);
-          const uint32_t ee = __shfl_sync(tmask, e, src);
-          const uint64_t ei = kLfu ? __shfl_sync(tmask, inc, src) : 0ull;
+        for (unsigned m = amask; m && r < F; m &= m - 1, ++r) {
+          const int i = __ffs(m) - 1;
+          pend &= ~(1u << i);
           if (pre <= r && r < pre + nf) {
-            const uint32_t slot = sub * 16 + (__fns(fm, 0, static_cast<int>(r - pre + 1)));
+            const uint32_t slot = sub * 16 + __fns(fm, 0, static_cast<int>(r - pre + 1));
             *reinterpret_cast<ulonglong2*>(key_at(t, row0 + slot)) =
-                make_ulonglong2(ke, score_of(ee, ei, false, 0ull));
-            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(ke)));
-            rslot[nrow] = static_cast<uint8_t>(slot);
-            ridx[nrow] = ee;
+                make_ulonglong2(ekey[i], escore[i]);
+            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(ekey[i])));
+            eslot[i] = static_cast<int32_t>(slot);
           }
-          ++nrow;
         }
-        if (sub == 0) n_adm += A;
-      } else if (evict) {
-        // full bucket, one or two incoming keys: the lane's two lowest
-        // (score, key) over its slots 8 i + sub
-        uint64_t s1 = ~0ull, k1 = ~0ull, s2 = ~0ull, k2 = ~0ull;
-        uint32_t l1 = kNone, l2 = kNone;
+      }
+      // ---- 4. evictions: E = the absent keys left
+      const uint32_t E = __popc(pend);
+      uint32_t evicted = 0;
+      if (E) {
+        __syncwarp(tmask);  // the placements and new scores are visible
+        // the slots free at entry (now holding keys of this call) rank as new:
+        // this lane's slots 8 q + sub lie in lane q/2's digest bytes
+        uint32_t newm = 0;  // bit q: slot 8 q + sub
 #pragma unroll
-        for (int g = 0; g < 16; g += 4) {
-          ulonglong2 p[4];
+        for (int l = 0; l < 8; ++l) {
+          const uint32_t f = __shfl_sync(tmask, fm, tb + l);
+          newm |= ((f >> sub) & 1u) << (2 * l);
+          newm |= ((f >> (8 + sub)) & 1u) << (2 * l + 1);
+        }
+        uint32_t removed = 0;  // bit q: slot 8 q + sub taken out
+        uint32_t nx = 0;       // slots taken out
+        for (uint32_t x = 0; x < E; ++x) {
+          uint64_t bs = ~0ull, bk = ~0ull;
+          uint32_t bn = 1u, bl = kNone;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            p[i] = *reinterpret_cast<const ulonglong2*>(key_at(t, row0 + 8 * (g + i) + sub));
+          for (int g = 0; g < 16; g += 4) {
+            ulonglong2 p[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t slot = 8 * (g + i) + sub;
-            if (sk_less(p[i].y, p[i].x, s2, k2)) {
-              if (sk_less(p[i].y, p[i].x, s1, k1)) {
-                s2 = s1;
-                k2 = k1;
-                l2 = l1;
-                s1 = p[i].y;
-                k1 = p[i].x;
-                l1 = slot;
-              } else {
-                s2 = p[i].y;
-                k2 = p[i].x;
-                l2 = slot;
+            for (int i = 0; i < 4; ++i)
+              p[i] = *reinterpret_cast<const ulonglong2*>(key_at(t, row0 + 8 * (g + i) + sub));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int q = g + i;
+              const uint32_t cn = (newm >> q) & 1u;
+              if (!((removed >> q) & 1u) &&
+                  (bl == kNone || rank3_less(p[i].y, cn, p[i].x, bs, bn, bk))) {
+                bs = p[i].y;
+                bk = p[i].x;
+                bn = cn;
+                bl = 8 * q + sub;
               }
             }
           }
-        }
-        // the bucket's lowest resident R0, and its second lowest R1 for two keys
-        uint64_t rs0 = s1, rk0 = k1, rs1 = ~0ull, rk1 = ~0ull;
-        uint32_t rl0 = l1, rl1 = kNone;
-        tile_min_sk(rs0, rk0, rl0, tmask);
-        if (A == 2) {
-          if (l1 == rl0) {
-            s1 = s2;
-            k1 = k2;
-            l1 = l2;
+          tile_min_rank(bs, bn, bk, bl, tmask);
+          // the lowest pending key (rank (score, 1, key)), if any is left
+          int pi = -1;
+          uint64_t ps = 0, pk = 0;
+          for (unsigned m = pend; m; m &= m - 1) {
+            const int i = __ffs(m) - 1;
+            if (pi < 0 || rank3_less(escore[i], 1u, ekey[i], ps, 1u, pk)) {
+              pi = i;
+              ps = escore[i];
+              pk = ekey[i];
+            }
           }
-          rs1 = s1;
-          rk1 = k1;
-          rl1 = l1;
-          tile_min_sk(rs1, rk1, rl1, tmask);
-        }
-        // the incoming keys P0 (and P1), in lane order
-        const unsigned src0 = tb + __ffs(am) - 1;
-        const unsigned src1 = A == 2 ? tb + __ffs(am & (am - 1)) - 1 : src0;
-        const uint64_t pk0 = __shfl_sync(tmask, key, src0), pk1 = __shfl_sync(tmask, key, src1);
-        const uint32_t pe0 = __shfl_sync(tmask, e, src0), pe1 = __shfl_sync(tmask, e, src1);
-        const uint64_t pi0 = kLfu ? __shfl_sync(tmask, inc, src0) : 0ull;
-        const uint64_t pi1 = kLfu ? __shfl_sync(tmask, inc, src1) : 0ull;
-        const uint64_t ps0 = score_of(pe0, pi0, false, 0ull), ps1 = score_of(pe1, pi1, false, 0ull);
-        // the A lowest ranks of {R0, .., P0, ..} go (residents rank (score, 0,
-        // key), incoming keys (score, 1, key)); R0 ranks below R1
-        bool gr0, gr1 = false, gp0, gp1 = false;
-        if (A == 1) {
-          gp0 = rank3_less(ps0, 1u, pk0, rs0, 0u, rk0);
-          gr0 = !gp0;
-        } else {
-          const uint32_t br0 = (rank3_less(ps0, 1u, pk0, rs0, 0u, rk0) ? 1u : 0u) +
-                               (rank3_less(ps1, 1u, pk1, rs0, 0u, rk0) ? 1u : 0u);
-          const uint32_t br1 = 1u + (rank3_less(ps0, 1u, pk0, rs1, 0u, rk1) ? 1u : 0u) +
-                               (rank3_less(ps1, 1u, pk1, rs1, 0u, rk1) ? 1u : 0u);
-          const bool p1lt0 = rank3_less(ps1, 1u, pk1, ps0, 1u, pk0);
-          const uint32_t bp0 = (rank3_less(rs0, 0u, rk0, ps0, 1u, pk0) ? 1u : 0u) +
-                               (rank3_less(rs1, 0u, rk1, ps0, 1u, pk0) ? 1u : 0u) + (p1lt0 ? 1u : 0u);
-          const uint32_t bp1 = (rank3_less(rs0, 0u, rk0, ps1, 1u, pk1) ? 1u : 0u) +
-                               (rank3_less(rs1, 0u, rk1, ps1, 1u, pk1) ? 1u : 0u) + (p1lt0 ? 0u : 1u);
-          gr0 = br0 < 2;
-          gr1 = br1 < 2;
-          gp0 = bp0 < 2;
-          gp1 = bp1 < 2;
-        }
-        // surviving incoming keys take the removed residents' slots: both, or
-        // the one survivor takes R0's
-        const uint32_t ev = (gr0 ? 1u : 0u) + (gr1 ? 1u : 0u);
-        const uint32_t rj = (gp0 ? 1u : 0u) + (gp1 ? 1u : 0u);
-        auto put = [&](uint32_t slot, uint64_t k, uint64_t sc, uint32_t ee) {
+          if (pi >= 0 && rank3_less(ps, 1u, pk, bs, bn, bk)) {
+            pend &= ~(1u << pi);  // rejected
+            continue;
+          }
+          // the slot goes: a key of this call placed there is displaced, a
+          // pre-call resident is evicted (also when this call updated it: a
+          // resident key's new score can still be the lowest), and no key of
+          // this call's row goes to it any more
+          if ((bl & 7u) == sub) removed |= 1u << (bl >> 3);
           if (sub == 0) {
-            *reinterpret_cast<ulonglong2*>(key_at(t, row0 + slot)) = make_ulonglong2(k, sc);
-            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(k)));
-            rslot[nrow] = static_cast<uint8_t>(slot);
-            ridx[nrow] = ee;
+            xslot[nx] = static_cast<uint8_t>(bl);
+            for (int i = 0; i < ne; ++i)
+              if (eslot[i] == static_cast<int32_t>(bl)) eslot[i] = -1;
           }
-          ++nrow;
-        };
-        if (ev == 2) {
-          put(rl0, pk0, ps0, pe0);
-          put(rl1, pk1, ps1, pe1);
-        } else if (ev == 1) {
-          if (!gp0) put(rl0, pk0, ps0, pe0);
-          else put(rl0, pk1, ps1, pe1);
+          ++nx;
+          if (!bn) ++evicted;
+          __syncwarp(tmask);
         }
-        if (sub == 0) {
-          n_adm += ev;
-          n_evi += ev;
-          n_rej += rj;
+        // the pending keys left take the removed slots, in order
+        uint32_t r = 0;
+        for (unsigned m = pend; m; m &= m - 1, ++r) {
+          const int i = __ffs(m) - 1;
+          const uint32_t slot = xslot[r];
+          if (sub == 0) {
+            *reinterpret_cast<ulonglong2*>(key_at(t, row0 + slot)) =
+                make_ulonglong2(ekey[i], escore[i]);
+            t.digests[row0 + slot] = static_cast<uint8_t>(digest_of_hash(hash64(ekey[i])));
+            eslot[i] = static_cast<int32_t>(slot);
+          }
         }
       }
-      // ---- the changed slots' value rows, four in flight
       __syncwarp(tmask);
+      // counts: absent keys resident at the end are admitted
+      uint32_t adm = 0;
+      for (unsigned m = amask; m; m &= m - 1) adm += eslot[__ffs(m) - 1] >= 0 ? 1u : 0u;
+      if (sub == 0) {
+        n_adm += adm;
+        n_rej += A - adm;
+        n_evi += evicted;
+      }
+      // ---- 5. the value rows of the keys resident at the end, four in flight
       float* const rows = row_ptr(t, row0);
-      for (uint32_t i = 0; i < nrow; i += 4) {
+      unsigned cm = 0;  // entries to copy
+      for (int i = 0; i < ne; ++i) cm |= eslot[i] >= 0 ? (1u << i) : 0u;
+      while (cm) {
         float* dst[4];
         const float* src[4];
         bool ok[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          ok[r] = i + r < nrow;
-          dst[r] = rows + (ok[r] ? rslot[i + r] : 0) * t.dim;
-          src[r] = values_in + static_cast<uint64_t>(ok[r] ? ridx[i + r] : 0) * t.dim;
+          ok[r] = cm != 0;
+          const int i = ok[r] ? __ffs(cm) - 1 : 0;
+          if (ok[r]) cm &= cm - 1;
+          dst[r] = rows + (ok[r] ? eslot[i] : 0) * t.dim;
+          src[r] = values_in + static_cast<uint64_t>(ok[r] ? eidx[i] : 0) * t.dim;
         }
         tile_copy_rows<4>(dst, src, ok, t.dim, sub, vec);
       }
-      __syncwarp(tmask);  // the row list is read before the next bucket writes it
+      __syncwarp(tmask);  // the lists are read before the next bucket writes them
     }
   }
+  const unsigned kFull = 0xFFFFFFFFu;
   const uint32_t u = __reduce_add_sync(kFull, n_upd), ad = __reduce_add_sync(kFull, n_adm);
   const uint32_t ev = __reduce_add_sync(kFull, n_evi), rj = __reduce_add_sync(kFull, n_rej);
   if (lane == 0) {
