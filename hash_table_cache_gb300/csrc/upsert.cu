@@ -1036,9 +1036,13 @@ __device__ __forceinline__ void tile_min_rank(uint64_t& s, uint32_t& nw, uint64_
   }
 }
 
-template <bool kLfu>
+// kDual: the buckets of a dual-mode pass (the keys routed to each bucket, all
+// absent; rank (score, key); keys the pass displaces go to the retry list
+// in the first pass (collect_retry); each bucket's summary is rewritten).
+template <bool kLfu, bool kDual>
 __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_kernel(
-    TableView t, UpsertScratch scr, const float* values_in, ScoreRule rule, bool vec) {
+    TableView t, UpsertScratch scr, const float* values_in, ScoreRule rule, bool vec,
+    bool collect_retry) {
   // per tile, its bucket's keys in stage order: key, batch index, increment,
   // score (absent keys), the slot a resident key holds or an absent key
   // ends in (-1: none), and a resident key's old score
@@ -1049,6 +1053,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
   __shared__ uint32_t eidx_sh[kTiles][kTileMaxEntries];
   __shared__ int32_t eslot_sh[kTiles][kTileMaxEntries];
   __shared__ uint8_t xslot_sh[kTiles][kTileMaxEntries];  // slots removed, in order
+  __shared__ uint32_t retry_sh[kTiles][kTileMaxEntries];  // dual: keys to route again
   pdl_wait();
   pdl_trigger();
   const unsigned lane = lane_id();
@@ -1062,6 +1067,8 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
   uint32_t* eidx = eidx_sh[tw];
   int32_t* eslot = eslot_sh[tw];
   uint8_t* xslot = xslot_sh[tw];
+  uint32_t* rtry = retry_sh[tw];
+  constexpr uint32_t kNew = kDual ? 0u : 1u;  // rank (score, new, key) or (score, key)
   auto score_of = [&](uint32_t e, uint64_t inc, bool resident, uint64_t old) -> uint64_t {
     if (kLfu) return policy_score(rule, e, inc, resident, old);
     return rule.in ? rule.in[e] : rule.clock;
@@ -1071,6 +1078,8 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
   const uint64_t nb = t.num_buckets;
   const uint64_t S = scr.map_size, smask = S - 1;
   uint32_t n_upd = 0, n_adm = 0, n_evi = 0, n_rej = 0;  // lane sub == 0 of each tile
+  int32_t n_net = 0;
+  uint32_t n_fill = 0;  // dual: net placements of the pass, free-slot placements
 
   // the tile's buckets tile, tile + T, ..., eight candidates per mark load
   for (uint64_t g0 = tile; g0 < nb; g0 += 8 * T) {
@@ -1084,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       const uint64_t lo = area_start(b, S, nb, scr.area_shift);
       const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
       uint64_t key[2], inc[2];
-      uint32_t raw[2];
+      uint32_t raw[2], bkt[2];
       unsigned stop = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -1092,14 +1101,16 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
         key[h] = scr.stage_keys[j & smask];
         raw[h] = scr.stage_idx[j & smask];
         inc[h] = kLfu ? scr.stage_inc[j & smask] : 0ull;
+        bkt[h] = kDual ? scr.stage_bkt[j & smask] : 0u;
         stop |= ((__ballot_sync(tmask, key[h] == kEmptyKey && j >= a_end) >> tb) & 0xFFu) << (8 * h);
       }
       const int end = stop ? __ffs(stop) - 1 : kTileRun;  // first position past the run
       unsigned em = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const bool mine = key[h] != kEmptyKey && static_cast<int>(8 * h + sub) < end &&
-                          bucket_of_hash(t, hash64(key[h])) == b;
+        const bool mine =
+            key[h] != kEmptyKey && static_cast<int>(8 * h + sub) < end &&
+            (kDual ? bkt[h] == static_cast<uint32_t>(b) : bucket_of_hash(t, hash64(key[h])) == b);
         em |= ((__ballot_sync(tmask, mine) >> tb) & 0xFFu) << (8 * h);
       }
       const int ne = __popc(em);
@@ -1120,8 +1131,15 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       __syncwarp(tmask);
       // ---- 2. look every key up (this lane: digest bytes of slots 16 sub ..)
       const uint4 dg = *reinterpret_cast<const uint4*>(t.digests + row0 + sub * 16);
-      unsigned hm = 0;  // entries resident
+      unsigned hm = 0;  // entries resident (none in dual mode: routed keys are absent)
       for (int i = 0; i < ne; ++i) {
+        if (kDual) {
+          if (sub == 0) {
+            eslot[i] = -1;
+            escore[i] = score_of(eidx[i], einc[i], false, 0ull);
+          }
+          continue;
+        }
         const uint64_t ke = ekey[i];
         const uint32_t pat = digest_of_hash(hash64(ke)) * 0x01010101u;
         uint32_t cm = byte_match4(dg.x, pat) | (byte_match4(dg.y, pat) << 4) |
@@ -1185,7 +1203,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       }
       // ---- 4. evictions: E = the absent keys left
       const uint32_t E = __popc(pend);
-      uint32_t evicted = 0;
+      uint32_t evicted = 0, displaced_earlier = 0, nretry = 0;
       if (E) {
         __syncwarp(tmask);  // the placements and new scores are visible
         // the slots free at entry (now holding keys of this call) rank as new:
@@ -1211,7 +1229,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int q = g + i;
-              const uint32_t cn = (newm >> q) & 1u;
+              const uint32_t cn = (newm >> q) & kNew;
               if (!((removed >> q) & 1u) &&
                   (bl == kNone || rank3_less(p[i].y, cn, p[i].x, bs, bn, bk))) {
                 bs = p[i].y;
@@ -1227,14 +1245,16 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
           uint64_t ps = 0, pk = 0;
           for (unsigned m = pend; m; m &= m - 1) {
             const int i = __ffs(m) - 1;
-            if (pi < 0 || rank3_less(escore[i], 1u, ekey[i], ps, 1u, pk)) {
+            if (pi < 0 || rank3_less(escore[i], kNew, ekey[i], ps, kNew, pk)) {
               pi = i;
               ps = escore[i];
               pk = ekey[i];
             }
           }
-          if (pi >= 0 && rank3_less(ps, 1u, pk, bs, bn, bk)) {
+          if (pi >= 0 && rank3_less(ps, kNew, pk, bs, bn, bk)) {
             pend &= ~(1u << pi);  // rejected
+            if (kDual && collect_retry && sub == 0) rtry[nretry] = eidx[pi];
+            ++nretry;
             continue;
           }
           // the slot goes: a key of this call placed there is displaced, a
@@ -1242,13 +1262,23 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
           // resident key's new score can still be the lowest), and no key of
           // this call's row goes to it any more
           if ((bl & 7u) == sub) removed |= 1u << (bl >> 3);
+          // placed by this pass (free at entry): a key of this call displaced
+          const bool fresh = (__shfl_sync(tmask, fm, tb + (bl >> 4)) >> (bl & 15u)) & 1u;
+          // dual mode's second pass: a key the first pass placed is also a
+          // key of this call
+          const bool earlier = kDual && !fresh && !collect_retry && absent_in_call(scr, bk);
           if (sub == 0) {
             xslot[nx] = static_cast<uint8_t>(bl);
-            for (int i = 0; i < ne; ++i)
-              if (eslot[i] == static_cast<int32_t>(bl)) eslot[i] = -1;
+            for (int i = 0; i < ne; ++i) {
+              if (eslot[i] != static_cast<int32_t>(bl)) continue;
+              eslot[i] = -1;
+              if (kDual && collect_retry && fresh) rtry[nretry] = eidx[i];
+            }
           }
+          if (kDual && collect_retry && fresh) ++nretry;
           ++nx;
-          if (!bn) ++evicted;
+          if (earlier) ++displaced_earlier;
+          else if (!fresh) ++evicted;
           __syncwarp(tmask);
         }
         // the pending keys left take the removed slots, in order
@@ -1268,7 +1298,46 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       // counts: absent keys resident at the end are admitted
       uint32_t adm = 0;
       for (unsigned m = amask; m; m &= m - 1) adm += eslot[__ffs(m) - 1] >= 0 ? 1u : 0u;
-      if (sub == 0) {
+      if (kDual) {
+        // the pass's net placements (keys of earlier passes of this call it
+        // displaced count against them), its free-slot placements, the keys
+        // to route again, and the bucket's new summary
+        const uint32_t placed_free = A < F ? A : F;
+        if (sub == 0) {
+          n_net += static_cast<int32_t>(adm) - static_cast<int32_t>(displaced_earlier);
+          n_fill += placed_free;
+        }
+        if (collect_retry && nretry) {
+          uint32_t at = 0;
+          if (sub == 0) at = atomicAdd(scr.cursor + 4, nretry);
+          at = __shfl_sync(tmask, at, tb);
+          for (uint32_t r = sub; r < nretry; r += 8) scr.retry[at + r] = rtry[r];
+        }
+        uint32_t cnt = 0;
+        uint64_t mn = ~0ull;
+#pragma unroll
+        for (int g = 0; g < 16; g += 4) {
+          ulonglong2 p[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            p[i] = *reinterpret_cast<const ulonglong2*>(key_at(t, row0 + 8 * (g + i) + sub));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (p[i].x == kEmptyKey) continue;
+            ++cnt;
+            mn = min(mn, static_cast<uint64_t>(p[i].y));
+          }
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+          cnt += __shfl_xor_sync(tmask, cnt, o);
+          mn = min(mn, static_cast<uint64_t>(__shfl_xor_sync(tmask, mn, o)));
+        }
+        if (sub == 0) {
+          t.summary[b].min_score = cnt ? mn : 0ull;
+          t.summary[b].count = cnt;
+        }
+      } else if (sub == 0) {
         n_adm += adm;
         n_rej += A - adm;
         n_evi += evicted;
@@ -1295,10 +1364,20 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
     }
   }
   const unsigned kFull = 0xFFFFFFFFu;
+  using ull = unsigned long long;
+  if (kDual) {  // dual_finish_kernel turns these into the call's counts
+    const int32_t net = __reduce_add_sync(kFull, n_net);
+    const uint32_t fills = __reduce_add_sync(kFull, n_fill);
+    if (lane == 0) {
+      if (fills) atomicAdd(&t.stats->fills, static_cast<ull>(fills));
+      if (net) atomicAdd(reinterpret_cast<ull*>(scr.cursor + 2),
+                         static_cast<ull>(static_cast<long long>(net)));
+    }
+    return;
+  }
   const uint32_t u = __reduce_add_sync(kFull, n_upd), ad = __reduce_add_sync(kFull, n_adm);
   const uint32_t ev = __reduce_add_sync(kFull, n_evi), rj = __reduce_add_sync(kFull, n_rej);
   if (lane == 0) {
-    using ull = unsigned long long;
     if (u) atomicAdd(&t.stats->updated, static_cast<ull>(u));
     if (ad) atomicAdd(&t.stats->admitted, static_cast<ull>(ad));
     if (ev) atomicAdd(&t.stats->evicted, static_cast<ull>(ev));
@@ -1828,11 +1907,13 @@ cudaError_t launch_bucket_pass(const TableView& t, const UpsertScratch& s, const
                                                            ex);
 }
 
-// The sparse-batch pass (single mode, plain insert_or_assign): the tile
-// kernel, then the general kernel on the buckets it deferred.
-cudaError_t launch_sparse_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
-                               const float* values, const ScoreRule& rule, bool vec,
-                               cudaStream_t st) {
+// The sparse-batch pass (single mode, plain insert_or_assign; and every pass
+// of dual mode): the tile kernel, then the general kernel on the buckets it
+// deferred.
+template <bool kDual>
+cudaError_t launch_tile_pass(const TableView& t, const UpsertScratch& s, const uint64_t* keys,
+                             const float* values, const ScoreRule& rule, bool vec, cudaStream_t st,
+                             bool collect_retry) {
   uint64_t blocks = (t.num_buckets * 8 + kThreads - 1) / kThreads;
   const uint64_t cap = static_cast<uint64_t>(sm_count()) * HKV_TILE_MIN_BLOCKS;
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
@@ -1842,14 +1923,15 @@ cudaError_t launch_sparse_pass(const TableView& t, const UpsertScratch& s, const
     if (rule.policy == kEpochLru) r.clock = rule.epoch_hi | (rule.clock & 0xFFFFFFFFull);
     r.policy = kCustomized;
   }
-  cudaError_t e =
-      rule.lfu()
-          ? launch_chained(upsert_tile_kernel<true>, grid, kThreads, 0, st, t, s, values, r, vec)
-          : launch_chained(upsert_tile_kernel<false>, grid, kThreads, 0, st, t, s, values, r, vec);
+  cudaError_t e = rule.lfu() ? launch_chained(upsert_tile_kernel<true, kDual>, grid, kThreads, 0,
+                                              st, t, s, values, r, vec, collect_retry)
+                             : launch_chained(upsert_tile_kernel<false, kDual>, grid, kThreads, 0,
+                                              st, t, s, values, r, vec, collect_retry);
   if (e != cudaSuccess) return e;
   UpsertExtra deferred;
   deferred.mark_want = kMarkDeferred;
-  return launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, deferred);
+  deferred.collect_retry = collect_retry;
+  return launch_bucket_pass<kDual>(t, s, keys, values, rule, vec, st, deferred);
 }
 
 }  // namespace
@@ -1876,7 +1958,7 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
                : launch_chained(stage_kernel<false>, sg, kThreads, 0, st, t, s, n, keys, inc_in);
     const bool plain = ex.update_resident && !ex.ev_keys;
     if (e == cudaSuccess && sparse && plain && HKV_UPSERT_SPARSE)
-      return launch_sparse_pass(t, s, keys, values, rule, vec, st);
+      return launch_tile_pass<false>(t, s, keys, values, rule, vec, st, false);
     if (e == cudaSuccess) e = launch_bucket_pass<false>(t, s, keys, values, rule, vec, st, ex);
     return e;
   }
@@ -1888,13 +1970,17 @@ cudaError_t launch_upsert(const TableView& t, const UpsertScratch& s, uint64_t n
                      n, keys, values, rule, vec);
   UpsertExtra first = ex;
   first.collect_retry = true;
-  if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, first);
+  if (e == cudaSuccess)
+    e = HKV_UPSERT_SPARSE ? launch_tile_pass<true>(t, s, keys, values, rule, vec, st, true)
+                          : launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, first);
   if (e == cudaSuccess)
     e = launch_chained(clear_scratch_kernel, grid_for(s.map_size / 2), kThreads, 0, st, s,
                        t.num_buckets, true);
   if (e == cudaSuccess)
     e = launch_chained(dual_retry_kernel, grid_for(n), kThreads, 0, st, t, s, keys, rule);
-  if (e == cudaSuccess) e = launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, ex);
+  if (e == cudaSuccess)
+    e = HKV_UPSERT_SPARSE ? launch_tile_pass<true>(t, s, keys, values, rule, vec, st, false)
+                          : launch_bucket_pass<true>(t, s, keys, values, rule, vec, st, ex);
   if (e != cudaSuccess) return e;
   dual_finish_kernel<<<1, 1, 0, st>>>(t, s);
   return cudaGetLastError();

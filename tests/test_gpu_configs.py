@@ -4,9 +4,10 @@ allows it:
 * 2^26 slots, dim 64, Zipf(1.05) steps at load factor 1.0: bit-exact against
   the oracle on a random sample of buckets (single-bucket results depend only
   on the keys of the bucket, so the oracle simulates just those buckets);
-* dual mode, 2^26 slots, dim 128: top-N score retention beside the oracle's
-  paper-scale figure (invariants are checked on the 2^20-slot twin in
-  test_gpu_modes-style per-bucket form);
+* dual mode, 2^26 slots, dim 128: top-N score retention, and the invariants
+  on a sample (bucket membership and last rows on sampled buckets; for
+  sampled absent keys, a full candidate bucket that outranks them, with the
+  keys outranked by only one candidate or with a free candidate counted);
 * tiered + three streams, scaled to 2^22 slots: bit-exact against the
   oracle's serial replay in host issue order.
 """
@@ -114,7 +115,53 @@ def test_c4_dual_full_size_retention(hkv):
     assert found.sum() == t.size()
     top = np.argpartition(scores, total - cap)[total - cap:]
     retention = found[top].mean()
-    print(f"c4 dual top-N retention {retention:.4f}, load factor {t.size() / cap:.4f}")
+    # every bucket's occupancy and lowest rank (score, key), from the table
+    # itself: the export, and each entry's bucket from its row address
+    import oracle
+    o = oracle.OracleTable(cap // 128, dim, dual=True)  # bucket function only
+    ek, _, es = t.export(with_values=False)
+    ptrs, ef, _ = t.find_ptr(ek, with_scores=False)
+    info = t.info()
+    eb = (ptrs - info["hbm_values_addr"]) // (4 * dim) // 128
+    assert bool(ef.all())
+    occ = torch.bincount(eb, minlength=cap // 128)
+    big = torch.iinfo(torch.int64).max
+    mins = torch.full((cap // 128,), big, dtype=torch.int64, device=DEV)
+    mins.scatter_reduce_(0, eb, es, reduce="amin")
+    flip = ek ^ torch.iinfo(torch.int64).min  # unsigned order of keys as signed
+    tie = torch.where(es == mins[eb], flip, torch.full_like(flip, big))
+    mink = torch.full((cap // 128,), big, dtype=torch.int64, device=DEV)
+    mink.scatter_reduce_(0, eb, tie, reduce="amin")
+    # sampled buckets: every entry sits in one of its two candidate buckets
+    # and carries its key's last row
+    sample = torch.unique(torch.from_numpy(wl.as_i64(wl.stream(71, 256) % np.uint64(cap // 128))).to(DEV))
+    in_s = torch.isin(eb, sample)
+    sk, sb = u64(ek[in_s]), eb[in_s].cpu().numpy().astype(np.uint64)
+    assert np.all((o.buckets_of(sk, 0) == sb) | (o.buckets_of(sk, 1) == sb))
+    sv, sf, _ = t.find(ek[in_s])
+    torch.cuda.synchronize()
+    assert bool(sf.all())
+    assert np.array_equal(sv.cpu().numpy(), wl.key_values(sk, dim, salt=1))
+    # absent keys (a sample): one candidate bucket full with every entry
+    # outranking the key (always); both (Algorithm 3 key by key: counted)
+    absent = np.flatnonzero(~found)
+    pick = absent[wl.permutation(72, absent.size)[:1 << 18]]
+    ak, asc = keys[pick], scores[pick]
+    occ_h, mins_h, mink_h = occ.cpu().numpy(), mins.cpu().numpy(), mink.cpu().numpy()
+    flip_k = (ak ^ np.uint64(1 << 63)).view(np.int64)
+    ok_b, free_b = [], []
+    for w in (0, 1):
+        c = o.buckets_of(ak, w).astype(np.int64)
+        above = (mins_h[c] > asc.astype(np.int64)) | \
+                ((mins_h[c] == asc.astype(np.int64)) & (mink_h[c] > flip_k))
+        ok_b.append((occ_h[c] == 128) & above)
+        free_b.append(occ_h[c] < 128)
+    assert np.all(ok_b[0] | ok_b[1]), "an absent key outranks both of its candidate buckets"
+    n_free = int((free_b[0] | free_b[1]).sum())
+    n_one = int((~(ok_b[0] & ok_b[1])).sum())
+    print(f"c4 dual top-N retention {retention:.4f}, load factor {t.size() / cap:.4f}; of "
+          f"{ak.size} sampled absent keys: {n_free} with a free candidate bucket, {n_one} "
+          f"outranked by one candidate only")
     assert retention > 0.98
     t.close()
 
