@@ -243,10 +243,10 @@ def rows_of_ptrs(ptrs, found, info):
 # dram__bytes_read.sum,dram__bytes_write.sum --clock-control none.
 # ---------------------------------------------------------------------------
 NCU_TRAFFIC = {
-    "find_kernel": {"bytes": None, "sources": ("find.cu", "common.cuh", "launch.h"),
-                    "sha256": ""},
-    "upsert_single_kernel": {"bytes": None, "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": ""},
+    "find_kernel": {"bytes": 269983915, "sources": ("find.cu", "common.cuh", "launch.h"),
+                    "sha256": "1df7e6ea41a8e232"},
+    "upsert_single_kernel": {"bytes": 330552405, "sources": ("upsert.cu", "common.cuh", "launch.h"),
+                             "sha256": "d0ec5e240dc8bd32"},
 }
 
 
@@ -726,9 +726,11 @@ def cfg_c1(ctx, steps, warmup, peak):
             "steps": steps, "gpu_launches_per_step": 4}
 
 
-def cfg_c3(ctx, steps, warmup, peak):
+def cfg_c3(ctx, steps, warmup, peak, small=False):
+    """small: 2^23 slots and 2^17-key batches (the same keys per bucket), a
+    size a full profiler capture handles."""
     torch, hkv = ctx.torch, ctx.hkv
-    cap, dim, n = 1 << 26, 64, 1 << 20
+    cap, dim, n = (1 << 23, 64, 1 << 17) if small else (1 << 26, 64, 1 << 20)
     t = hkv.HashTable(cap, dim, device=ctx.local)
     keys = wl.unique_keys(6, int(1.6 * cap))
     fill_table(ctx, t, cap, 0, keys, dim, batch=1 << 20)
@@ -742,6 +744,8 @@ def cfg_c3(ctx, steps, warmup, peak):
         f = ctx.dk(wl.zipf_keys(10007 + s, n, 1.05, 1 << 32))
         c0 = t.op_counts()
         uv = wl.key_values_torch(u, dim, salt=100 + s)
+        if s == warmup:
+            torch.cuda.nvtx.range_push("timed")  # lets a profiler select the timed steps
         ctx.flush.zero_()
         a, b, c = ctx.ev(), ctx.ev(), ctx.ev()
         a.record(ctx.stream)
@@ -760,6 +764,7 @@ def cfg_c3(ctx, steps, warmup, peak):
             fb.append(find_bytes_per_key(dim, h) * n)
             uniq.append(int(torch.unique(u).numel()))
             hits.append(h)
+    torch.cuda.nvtx.range_pop()
     t.close()
     u, f = statistics.mean(up), statistics.mean(fi)
     return {"value": 2 * n / (u + f) / 1e9, "ms_per_step": (u + f) * 1e3,
@@ -770,27 +775,35 @@ def cfg_c3(ctx, steps, warmup, peak):
             "steps": steps, "gpu_launches_per_step": 4}
 
 
-def cfg_c4(ctx, steps, warmup, peak, full_stream=True):
+def cfg_c4(ctx, steps, warmup, peak, small=False):
     """Dual mode: the 1.5 x capacity insert stream (every batch timed), the
-    retention of the top-N scores after it, then finds of inserted keys."""
+    retention of the top-N scores after it, then finds of inserted keys.
+    small: 2^23 slots and 2^17-key batches (the same keys per bucket); the
+    batches at load factor 1.0 run inside an NVTX range "timed"."""
     torch, hkv = ctx.torch, ctx.hkv
-    cap, dim, n = 1 << 26, 128, 1 << 20
+    cap, dim, n = (1 << 23, 128, 1 << 17) if small else (1 << 26, 128, 1 << 20)
     nb = cap // 128
     t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_DUAL, device=ctx.local)
     total = int(1.5 * cap)
     keys = wl.unique_keys(8, total)
     scores = wl.stream(9, total) >> np.uint64(2)
     up_t, up_b, lam1 = [], [], []
+    in_range = False
     for i, p in enumerate(range(0, total, n)):
         k = ctx.dk(keys[p:p + n])
         sc = ctx.dk(scores[p:p + n])
         v = wl.key_values_torch(k, dim, salt=1)
         c0 = t.op_counts()
+        if not in_range and t.size() >= cap:
+            torch.cuda.nvtx.range_push("timed")  # the batches at load factor 1.0
+            in_range = True
         dt = ctx.timed(lambda: t.insert_or_assign(k, v, sc))
         cnt = {kk: vv - c0[kk] for kk, vv in t.op_counts().items()}
         up_t.append(dt)
         up_b.append(upsert_bytes_paths(cnt, k.numel(), dim, dual=True))
         lam1.append(cnt["evicted"] + cnt["rejected"] > 0)
+    if in_range:
+        torch.cuda.nvtx.range_pop()
     # top-N retention (HKV §5.5, Table 11): resident keys among the N = capacity
     # highest scores of all inserted keys (scores are distinct)
     thr = np.partition(scores, total - cap)[total - cap]
@@ -1052,9 +1065,9 @@ def run_other(args):
     if cfg == "c1":
         r = cfg_c1(ctx, args.steps, args.warmup, peak)
     elif cfg == "c3":
-        r = cfg_c3(ctx, args.steps, args.warmup, peak)
+        r = cfg_c3(ctx, args.steps, args.warmup, peak, small=args.small)
     elif cfg == "c4":
-        r = cfg_c4(ctx, args.steps, args.warmup, peak)
+        r = cfg_c4(ctx, args.steps, args.warmup, peak, small=args.small)
     else:
         r = cfg_c5(ctx, args.steps, args.warmup, peak, probe_host_link(4 * 64))
     line = {
@@ -1063,6 +1076,8 @@ def run_other(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u64 keys/scores, f32 values (copied)", "data": "synthetic",
         "config": {"workload": OTHER[cfg], "name": cfg,
+                   "scale": "2^23 slots, 2^17-key batches" if args.small and cfg in ("c3", "c4")
+                   else "full",
                    "l2": "flushed before each timed call or step, outside the events"},
         "result": r,
     }
@@ -1263,6 +1278,28 @@ def run_ablation(args):
                       **res, "default_over_variant": {k: a[k] / b[k] for k in a}}))
 
 
+def run_probe_sweep():
+    """Random reads of 32..512-byte granules over a 4 GiB buffer at 1..16
+    reads in flight and 2, 4, 8 blocks per SM (G reads/s), and the host link
+    by SM loads and stores (GB/s)."""
+    import ctypes
+
+    import torch
+    torch.cuda.init()
+    lib = _probe_lib()
+    grid = {}
+    for g in (32, 64, 128, 256, 512):
+        for b in (2, 4, 8):
+            for d in (1, 2, 4, 8, 16):
+                if g >= 256 and d == 16:
+                    continue  # 64 registers of rows per lane
+                r = ctypes.c_double(0.0)
+                st = lib.hkv_probe_random_reads_at(g, 4 << 30, d, b, ctypes.byref(r))
+                grid[f"{g}B blocks={b} depth={d}"] = round(r.value / 1e9, 2) if st == 0 else None
+    link = {k: (round(v / 1e9, 1) if v else None) for k, v in probe_host_link(256).items()}
+    print(json.dumps({"random_reads_G_per_s": grid, "host_link_GB_per_s": link}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1278,13 +1315,21 @@ def main():
                     help="timed steps of each other workload in the headline line")
     ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"],
                     help="workload; c2 (the default) is the headline line")
+    ap.add_argument("--small", action="store_true",
+                    help="c3, c4: 2^23 slots and 2^17-key batches (the same keys per bucket; "
+                         "for profiler captures)")
+    ap.add_argument("--probe-sweep", action="store_true",
+                    help="print the random-read rates of this GPU over granule, reads in flight "
+                         "and blocks per SM, and the host link by SM access, as one JSON object")
     ap.add_argument("--ablation", choices=["digest", "pipeline"],
                     help="compare the default build with a variant build instead: find without "
                          "the digest line, or the pipelined bucket kernel")
     ap.add_argument("--ablation-child", help=argparse.SUPPRESS)
     ap.add_argument("--ablation-what", default="find", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    if args.ablation_child:
+    if args.probe_sweep:
+        run_probe_sweep()
+    elif args.ablation_child:
         run_ablation_child(args.ablation_child, args.ablation_what)
     elif args.ablation:
         run_ablation(args)
