@@ -53,7 +53,8 @@ constexpr int kBucketThreads = HKV_BUCKET_THREADS;  // bucket kernel block size
 #define HKV_UPSERT_PREFETCH 1
 #endif
 // sparse batches (at most 4 keys per bucket) of plain insert_or_assign take
-// the register-resident bucket pass (upsert_sparse_kernel)
+// the tile-per-bucket pass (upsert_tile_kernel); 0 sends every batch to the
+// warp-per-bucket kernel
 #ifndef HKV_UPSERT_SPARSE
 #define HKV_UPSERT_SPARSE 1
 #endif
@@ -1015,6 +1016,10 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
 #define HKV_TILE_MIN_BLOCKS 4
 #endif
 constexpr uint8_t kMarkDeferred = 2;
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 constexpr int kTileRun = 16;       // stage positions a tile reads, two per lane
 constexpr int kTileMaxEntries = 8;  // keys per bucket the tile path takes
 
@@ -1089,6 +1094,10 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       const uint64_t b = g0 + (__ffs(todo) - 1) * T;
       todo &= todo - 1;
       const uint64_t row0 = b * kSlots;
+      // the bucket's (key, score) pairs into L1 now: the candidate checks and
+      // the eviction rounds read them after the stage and digest loads
+      prefetch_l1(key_at(t, row0 + 16 * sub));
+      prefetch_l1(key_at(t, row0 + 16 * sub + 8));
       // ---- 1. the bucket's keys: stage positions lo + sub and lo + 8 + sub
       const uint64_t lo = area_start(b, S, nb, scr.area_shift);
       const uint64_t a_end = area_start(b + 1, S, nb, scr.area_shift);
@@ -1106,12 +1115,14 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
       }
       const int end = stop ? __ffs(stop) - 1 : kTileRun;  // first position past the run
       unsigned em = 0;
+      uint64_t sin[2];  // non-LFU rules: the score of each of this lane's keys
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const bool mine =
             key[h] != kEmptyKey && static_cast<int>(8 * h + sub) < end &&
             (kDual ? bkt[h] == static_cast<uint32_t>(b) : bucket_of_hash(t, hash64(key[h])) == b);
         em |= ((__ballot_sync(tmask, mine) >> tb) & 0xFFu) << (8 * h);
+        sin[h] = (!kLfu && mine && rule.in) ? rule.in[(raw[h] & ~kHitMark) - 1] : rule.clock;
       }
       const int ne = __popc(em);
       if (!stop || ne > kTileMaxEntries) {  // a long run or many keys: general kernel
@@ -1126,6 +1137,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
           ekey[i] = key[h];
           eidx[i] = (raw[h] & ~kHitMark) - 1;
           einc[i] = inc[h];
+          if (!kLfu) escore[i] = sin[h];
         }
       }
       __syncwarp(tmask);
@@ -1136,7 +1148,7 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
         if (kDual) {
           if (sub == 0) {
             eslot[i] = -1;
-            escore[i] = score_of(eidx[i], einc[i], false, 0ull);
+            if (kLfu) escore[i] = score_of(eidx[i], einc[i], false, 0ull);
           }
           continue;
         }
@@ -1161,11 +1173,11 @@ __global__ void __launch_bounds__(kThreads, HKV_TILE_MIN_BLOCKS) upsert_tile_ker
           hm |= 1u << i;
           if (sub == static_cast<unsigned>(__ffs(hb) - 1)) {  // the lane that found it
             eslot[i] = hs;
-            *score_at(t, row0 + hs) = score_of(eidx[i], einc[i], true, old);
+            *score_at(t, row0 + hs) = kLfu ? score_of(eidx[i], einc[i], true, old) : escore[i];
           }
         } else if (sub == 0) {
           eslot[i] = -1;
-          escore[i] = score_of(eidx[i], einc[i], false, 0ull);
+          if (kLfu) escore[i] = score_of(eidx[i], einc[i], false, 0ull);
         }
       }
       const uint32_t nh = __popc(hm);
@@ -1518,20 +1530,16 @@ __device__ __forceinline__ void tile_probe_pair_many(const TableView& t, const u
   }
 }
 
-// Dual-mode pass 1 and assign take 32 consecutive keys per warp: the dedup
-// lookup and the per-key follow-up run one key per lane, so a warp keeps 32
-// keys' accesses in flight; the bucket probe (both candidate lines with
-// kPair) runs on the warp's four 8-lane tiles, each probing the keys of its
-// own 8 lanes, U at a time, and copying the input rows of the resident ones
-// over their table rows.  Result: the lane's own key's
-// slot (or -1) and bucket.  `live` selects the lanes whose key is probed.
-#ifndef HKV_ROUTE_KEYS_PER_TILE
-#define HKV_ROUTE_KEYS_PER_TILE 1
-#endif
+// assign takes 32 consecutive keys per warp: the dedup lookup and the
+// per-key follow-up run one key per lane, so a warp keeps 32 keys' accesses
+// in flight; the bucket probe (both candidate lines with kPair) runs on the
+// warp's four 8-lane tiles, each probing the keys of its own 8 lanes, U at a
+// time, and copying the input rows of the resident ones over their table
+// rows.  Result: the lane's own key's slot (or -1) and bucket.  `live`
+// selects the lanes whose key is probed.
 #ifndef HKV_ASSIGN_KEYS_PER_TILE
 #define HKV_ASSIGN_KEYS_PER_TILE 1
 #endif
-constexpr int kRouteKeysPerTile = HKV_ROUTE_KEYS_PER_TILE;
 constexpr int kAssignKeysPerTile = HKV_ASSIGN_KEYS_PER_TILE;
 
 template <bool kPair, int U>
@@ -1598,14 +1606,97 @@ __device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k,
 #define HKV_ASSIGN_MIN_BLOCKS 6
 #endif
 #ifndef HKV_ROUTE_MIN_BLOCKS
-#define HKV_ROUTE_MIN_BLOCKS 6
+#define HKV_ROUTE_MIN_BLOCKS 4
 #endif
+
+// Candidate mask of 16 digest bytes: bit j set when byte j may equal the
+// key's digest (`pat` = digest * 0x01010101).
+__device__ __forceinline__ uint32_t digest_mask16(const uint4& dg, uint32_t pat) {
+  return byte_match4(dg.x, pat) | (byte_match4(dg.y, pat) << 4) | (byte_match4(dg.z, pat) << 8) |
+         (byte_match4(dg.w, pat) << 12);
+}
+
+// Removes and returns the lowest set bit of a 128-bit slot mask (-1: empty).
+__device__ __forceinline__ int take_slot(uint4& m) {
+  if (m.x) {
+    const int b = __ffs(m.x) - 1;
+    m.x &= m.x - 1;
+    return b;
+  }
+  if (m.y) {
+    const int b = __ffs(m.y) - 1;
+    m.y &= m.y - 1;
+    return 32 + b;
+  }
+  if (m.z) {
+    const int b = __ffs(m.z) - 1;
+    m.z &= m.z - 1;
+    return 64 + b;
+  }
+  if (m.w) {
+    const int b = __ffs(m.w) - 1;
+    m.w &= m.w - 1;
+    return 96 + b;
+  }
+  return -1;
+}
+
+// Candidate slots of the warp's probing keys in both of their buckets (HKV
+// §3.4: two fixed-length line loads per key): tile j loads the two digest
+// lines of each of keys 8j..8j+7, two keys' four lines in flight, and each
+// key's two 128-bit masks reach its lane through `msk` (32 keys x 16 x 16
+// bits: b1's line, then b2's).  Read-only loads: no thread of the route
+// kernel writes digests.
+__device__ __forceinline__ void route_candidates(const TableView& t, unsigned probe, uint32_t b1,
+                                                 uint32_t b2, uint32_t pat, unsigned lane,
+                                                 uint16_t (*msk)[16], uint4& c1, uint4& c2) {
+  constexpr unsigned kFull = 0xFFFFFFFFu;
+  const unsigned tile = lane >> 3, sub = lane & 7u;
+#pragma unroll
+  for (int g = 0; g < 8; g += 2) {
+    uint4 d1[2], d2[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const unsigned src = tile * 8 + g + m;
+      const uint32_t x1 = __shfl_sync(kFull, b1, src);
+      const uint32_t x2 = __shfl_sync(kFull, b2, src);
+      if ((probe >> src) & 1u) {
+        d1[m] = ld_nc_v4(t.digests + static_cast<uint64_t>(x1) * kSlots + sub * 16);
+        d2[m] = ld_nc_v4(t.digests + static_cast<uint64_t>(x2) * kSlots + sub * 16);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const unsigned src = tile * 8 + g + m;
+      const uint32_t p = __shfl_sync(kFull, pat, src);
+      const bool on = (probe >> src) & 1u;
+      msk[src][sub] = static_cast<uint16_t>(on ? digest_mask16(d1[m], p) : 0u);
+      msk[src][8 + sub] = static_cast<uint16_t>(on ? digest_mask16(d2[m], p) : 0u);
+    }
+  }
+  __syncwarp();
+  c1 = *reinterpret_cast<const uint4*>(&msk[lane][0]);
+  c2 = *reinterpret_cast<const uint4*>(&msk[lane][8]);
+  __syncwarp();  // every lane has its masks before the next probe writes them
+}
+
+// A warp takes 32 consecutive keys, one per lane for everything scalar (the
+// dedup lookup, hash, candidate confirmation, score update, routing and
+// staging), so the 32 keys' accesses are in flight together; the 128-byte
+// transfers (digest lines, value rows) run on the four 8-lane tiles.  The
+// two bucket summaries of each key are brought into L2 at the start, for
+// the routing of the keys found absent.
 __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
     ScoreRule rule, bool vec) {
+  __shared__ __align__(16) uint16_t masks_sh[kThreads / 32][32][16];
   pdl_wait();
   pdl_trigger();
+  constexpr unsigned kFull = 0xFFFFFFFFu;
   const unsigned lane = lane_id();
+  const unsigned tile = lane >> 3, sub = lane & 7u;
+  const unsigned tmask = 0xFFu << (tile * 8);
+  uint16_t(*msk)[16] = masks_sh[threadIdx.x >> 5];
   const uint64_t warps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   unsigned long long upd = 0, absent = 0;
   for (uint64_t base = ((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 32;
@@ -1615,22 +1706,81 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
     const uint32_t ms = i < n && !is_reserved(k) ? map_last_occurrence(sc, k, i) : kNone;
     const bool live = ms != kNone;  // the key's last occurrence in the batch
     const uint64_t h = hash64(k);
-    const uint64_t b1 = bucket_of_hash(t, h);
-    const uint64_t b2 = bucket2_of(t, k, b1);
-    uint64_t b;
-    const int slot =
-        warp_probe_update<true, kRouteKeysPerTile>(t, k, h, b1, b2, live, values, base, vec, b);
-    if (!live) continue;
-    sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
-    const uint64_t inc = entry_inc(sc, ms);
-    if (slot >= 0) {
-      uint64_t* sp = score_at(t, b * kSlots + static_cast<uint64_t>(slot));
-      *sp = policy_score(rule, i, inc, true, rule.lfu() ? *sp : 0ull);
-      ++upd;
-    } else {
-      ++absent;
-      const uint64_t target = route_bucket(t, b1, b2, policy_score(rule, i, inc, false, 0));
-      if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
+    const uint32_t b1 = static_cast<uint32_t>(bucket_of_hash(t, h));
+    const uint32_t b2 = static_cast<uint32_t>(bucket2_of(t, k, b1));
+    if (live) {
+      prefetch_l2(t.summary + b1);
+      prefetch_l2(t.summary + b2);
+    }
+    const unsigned probe = __ballot_sync(kFull, live);
+    if (!probe) continue;
+    uint4 c1, c2;
+    route_candidates(t, probe, b1, b2, digest_of_hash(h) * 0x01010101u, lane, msk, c1, c2);
+    // confirm: the first candidate of each bucket in flight together, then
+    // the rest (rare) in order; a key sits in at most one of its buckets
+    int slot = -1;
+    uint32_t bk = b1;
+    if (live) {
+      const int a1 = take_slot(c1), a2 = take_slot(c2);
+      uint64_t k1 = 0, k2 = 0;
+      if (a1 >= 0) k1 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + a1));
+      if (a2 >= 0) k2 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + a2));
+      if (a1 >= 0 && k1 == k) {
+        slot = a1;
+      } else if (a2 >= 0 && k2 == k) {
+        slot = a2;
+        bk = b2;
+      } else {
+        for (int c = take_slot(c1); c >= 0; c = take_slot(c1)) {
+          if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + c)) == k) {
+            slot = c;
+            break;
+          }
+        }
+        if (slot < 0) {
+          for (int c = take_slot(c2); c >= 0; c = take_slot(c2)) {
+            if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + c)) == k) {
+              slot = c;
+              bk = b2;
+              break;
+            }
+          }
+        }
+      }
+    }
+    if (live) {
+      sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
+      const uint64_t inc = entry_inc(sc, ms);
+      if (slot >= 0) {
+        uint64_t* sp = score_at(t, static_cast<uint64_t>(bk) * kSlots + static_cast<uint64_t>(slot));
+        *sp = policy_score(rule, i, inc, true, rule.lfu() ? *sp : 0ull);
+        ++upd;
+      } else {
+        ++absent;
+        const uint64_t target = route_bucket(t, b1, b2, policy_score(rule, i, inc, false, 0));
+        if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
+      }
+    }
+    // resident keys: tile j copies the input rows of keys 8j..8j+7 over
+    // their table rows, two rows in flight (more hold registers the
+    // rest of the kernel needs)
+    unsigned rows = (__ballot_sync(kFull, slot >= 0) >> (tile * 8)) & 0xFFu;
+    while (rows) {
+      float* dst[2];
+      const float* src[2];
+      bool ok[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        ok[r] = rows != 0;
+        const unsigned j = ok[r] ? __ffs(rows) - 1 : 0u;
+        if (ok[r]) rows &= rows - 1;
+        const unsigned from = tile * 8 + j;
+        const int s_ = __shfl_sync(tmask, slot, from);
+        const uint32_t b_ = __shfl_sync(tmask, bk, from);
+        dst[r] = ok[r] ? row_ptr(t, static_cast<uint64_t>(b_) * kSlots + s_) : nullptr;
+        src[r] = ok[r] ? values + (base + from) * t.dim : values;
+      }
+      tile_copy_rows<2>(dst, src, ok, t.dim, sub, vec);
     }
   }
   warp_add(&t.stats->updated, upd);

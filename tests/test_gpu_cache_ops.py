@@ -82,6 +82,19 @@ def test_contains_and_find_ptr(hkv, oracle_mod, mode):
         ov, of, os_ = gv_.cpu().numpy(), gf_.cpu().numpy(), u64(gs_)
         rk = set(u64(t.export(with_values=False)[0]).tolist())
         assert np.array_equal(of.astype(bool), np.array([int(x) in rk for x in q]))
+        # independent of the GPU: keys never inserted are not found, a found
+        # key carries the value and score it was inserted with, and every
+        # resident key (all of them inserted keys, every other one queried)
+        # is found
+        n_ins = keys[::2].size
+        assert not of[n_ins:].any()
+        pos = {int(k): j for j, k in enumerate(keys)}
+        src = np.array([pos[int(x)] for x in q[:n_ins]])
+        fi = np.flatnonzero(of[:n_ins])
+        assert np.array_equal(ov[fi].view(np.uint32), vals[src[fi]].view(np.uint32))
+        assert np.array_equal(os_[fi], sc[src[fi]])
+        assert len(rk) == t.size() and rk <= set(int(k) for k in keys)
+        assert of[:n_ins].sum() == len(rk & set(int(k) for k in keys[::2]))
     else:
         ov, of, os_ = o.find(q)
     gf = t.contains(dkeys(q))
