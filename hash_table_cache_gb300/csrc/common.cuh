@@ -372,119 +372,4 @@ __device__ __forceinline__ int tile_probe(const TableView& t, uint64_t b, uint64
   return __shfl_sync(tmask, hit, __ffs(bal) - 1);
 }
 
-// Probe both candidate buckets of a dual-mode key at once (HKV §3.4: two
-// fixed-length line loads): the two digest lines are loaded together, then
-// the candidates of b1 and of b2 are confirmed.  Returns the slot and sets
-// `b` to the bucket holding the key, or returns -1.
-template <bool kNC>
-__device__ __forceinline__ int tile_probe_pair(const TableView& t, uint64_t b1, uint64_t b2,
-                                               uint64_t key, uint32_t pat, unsigned sub,
-                                               unsigned tmask, uint64_t& b) {
-  const uint8_t* d1 = t.digests + b1 * kSlots + sub * 16;
-  const uint8_t* d2 = t.digests + b2 * kSlots + sub * 16;
-  uint4 g1, g2;
-  if (kNC) {
-    g1 = ld_nc_v4(d1);
-    g2 = ld_nc_v4(d2);
-  } else {
-    g1 = ld_cg_v4(d1);
-    g2 = ld_cg_v4(d2);
-  }
-  uint32_t m1 = byte_match4(g1.x, pat) | (byte_match4(g1.y, pat) << 4) |
-                (byte_match4(g1.z, pat) << 8) | (byte_match4(g1.w, pat) << 12);
-  uint32_t m2 = byte_match4(g2.x, pat) | (byte_match4(g2.y, pat) << 4) |
-                (byte_match4(g2.z, pat) << 8) | (byte_match4(g2.w, pat) << 12);
-  int hit = -1;
-  uint32_t which = 0;
-  const uint64_t* k1 = t.slots + 2 * (b1 * kSlots + sub * 16);
-  const uint64_t* k2 = t.slots + 2 * (b2 * kSlots + sub * 16);
-  while (m1 | m2) {
-    const bool first = m1 != 0;
-    uint32_t& m = first ? m1 : m2;
-    const int bit = __ffs(m) - 1;
-    m &= m - 1;
-    const uint64_t* kp = (first ? k1 : k2) + 2 * bit;
-    const uint64_t kk = kNC ? ld_nc_u64(kp) : ld_cg_u64(kp);
-    if (kk == key) {
-      hit = static_cast<int>(sub * 16 + bit);
-      which = first ? 1u : 2u;
-      break;
-    }
-  }
-  // a key sits in at most one of its buckets
-  const unsigned bal = __ballot_sync(tmask, hit >= 0) & tmask;
-  if (!bal) return -1;
-  const int lead = __ffs(bal) - 1;
-  which = __shfl_sync(tmask, which, lead);
-  b = which == 1u ? b1 : b2;
-  return __shfl_sync(tmask, hit, lead);
-}
-
-// Probe bucket b[u] for key k[u], u < U, with the 8 lanes of a tile, all at
-// once: the U digest-line loads, then the U first-match (key, score) pair
-// loads, are issued back to back so a tile keeps U requests in flight.
-// Returns the slot (or -1) and, on a hit, the score, which comes with the key
-// in the same 16-byte load.  Read-only loads: the callers write no key or
-// digest.
-template <int U>
-__device__ __forceinline__ void tile_probe_many(const TableView& t, const uint64_t (&b)[U],
-                                                const uint64_t (&k)[U], const uint32_t (&pat)[U],
-                                                const bool (&act)[U], unsigned sub, unsigned tmask,
-                                                int (&slot)[U],
-                                                uint64_t (&score)[U]) {
-  uint4 dg[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-    if (act[u]) dg[u] = ld_nc_v4(t.digests + b[u] * kSlots + sub * 16);
-  uint32_t m[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    m[u] = 0;
-    if (act[u])
-      m[u] = byte_match4(dg[u].x, pat[u]) | (byte_match4(dg[u].y, pat[u]) << 4) |
-             (byte_match4(dg[u].z, pat[u]) << 8) | (byte_match4(dg[u].w, pat[u]) << 12);
-  }
-  ulonglong2 kk[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (m[u]) {
-      const uint64_t row = b[u] * kSlots + sub * 16 + (__ffs(m[u]) - 1);
-      kk[u] = ld_nc_pair(key_at(t, row));
-    }
-  }
-  int hit[U];
-  uint64_t hs[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    hit[u] = -1;
-    hs[u] = 0;
-    if (m[u]) {
-      int bit = __ffs(m[u]) - 1;
-      if (kk[u].x == k[u]) {
-        hit[u] = static_cast<int>(sub * 16 + bit);
-        hs[u] = kk[u].y;
-      } else {
-        m[u] &= m[u] - 1;
-        while (m[u]) {  // further digest matches (rare)
-          bit = __ffs(m[u]) - 1;
-          m[u] &= m[u] - 1;
-          const ulonglong2 p = ld_nc_pair(key_at(t, b[u] * kSlots + sub * 16 + bit));
-          if (p.x == k[u]) {
-            hit[u] = static_cast<int>(sub * 16 + bit);
-            hs[u] = p.y;
-            break;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
-    const int lead = bal ? __ffs(bal) - 1 : static_cast<int>(lane_id());
-    slot[u] = bal ? __shfl_sync(tmask, hit[u], lead) : -1;
-    score[u] = __shfl_sync(tmask, hs[u], lead);
-  }
-}
-
 }  // namespace hkv

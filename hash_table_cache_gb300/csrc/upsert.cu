@@ -1457,153 +1457,10 @@ __device__ __forceinline__ void stage_routed(const TableView& t, const UpsertScr
   sc.mark[target] = 1;
 }
 
-// Probe both candidate buckets of U dual-mode keys with the 8 lanes of a tile
-// (HKV §3.4: two fixed-length line loads per key): the 2U digest lines are
-// loaded together, then every key's first digest match is confirmed, those
-// key loads in flight together too.  slot[u] is the slot or -1, bkt[u] the
-// bucket holding the key; uniform across the tile.  Read-only loads: no
-// thread of the calling kernels writes keys or digests.
-template <int U>
-__device__ __forceinline__ void tile_probe_pair_many(const TableView& t, const uint64_t (&b1)[U],
-                                                     const uint64_t (&b2)[U],
-                                                     const uint64_t (&k)[U],
-                                                     const uint32_t (&pat)[U],
-                                                     const bool (&act)[U], unsigned sub,
-                                                     unsigned tmask, int (&slot)[U],
-                                                     uint64_t (&bkt)[U]) {
-  uint4 g1[U], g2[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (act[u]) {
-      g1[u] = ld_nc_v4(t.digests + b1[u] * kSlots + sub * 16);
-      g2[u] = ld_nc_v4(t.digests + b2[u] * kSlots + sub * 16);
-    }
-  }
-  // bits 0-15: the lane's 16 bytes of b1's line; bits 16-31: of b2's
-  uint32_t m[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    m[u] = 0;
-    if (act[u])
-      m[u] = byte_match4(g1[u].x, pat[u]) | (byte_match4(g1[u].y, pat[u]) << 4) |
-             (byte_match4(g1[u].z, pat[u]) << 8) | (byte_match4(g1[u].w, pat[u]) << 12) |
-             (byte_match4(g2[u].x, pat[u]) << 16) | (byte_match4(g2[u].y, pat[u]) << 20) |
-             (byte_match4(g2[u].z, pat[u]) << 24) | (byte_match4(g2[u].w, pat[u]) << 28);
-  }
-  auto key_ptr = [&](int u, int bit) {
-    const uint64_t b = bit < 16 ? b1[u] : b2[u];
-    return key_at(t, b * kSlots + sub * 16 + static_cast<uint32_t>(bit & 15));
-  };
-  uint64_t first[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-    if (m[u]) first[u] = ld_nc_u64(key_ptr(u, __ffs(m[u]) - 1));
-  int hit[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    hit[u] = -1;
-    if (!m[u]) continue;
-    int bit = __ffs(m[u]) - 1;
-    if (first[u] == k[u]) {
-      hit[u] = bit;
-      continue;
-    }
-    m[u] &= m[u] - 1;
-    while (m[u]) {  // further digest matches (rare)
-      bit = __ffs(m[u]) - 1;
-      m[u] &= m[u] - 1;
-      if (ld_nc_u64(key_ptr(u, bit)) == k[u]) {
-        hit[u] = bit;
-        break;
-      }
-    }
-  }
-  // a key sits in at most one of its buckets: code = slot, +128 for b2
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const unsigned bal = __ballot_sync(tmask, hit[u] >= 0) & tmask;
-    int code = hit[u] < 0 ? -1
-                          : static_cast<int>(sub * 16) + (hit[u] & 15) + ((hit[u] & 16) ? 128 : 0);
-    code = bal ? __shfl_sync(tmask, code, __ffs(bal) - 1) : -1;
-    slot[u] = code < 0 ? -1 : (code & 127);
-    bkt[u] = code >= 128 ? b2[u] : b1[u];
-  }
-}
-
-// assign takes 32 consecutive keys per warp: the dedup lookup and the
-// per-key follow-up run one key per lane, so a warp keeps 32 keys' accesses
-// in flight; the bucket probe (both candidate lines with kPair) runs on the
-// warp's four 8-lane tiles, each probing the keys of its own 8 lanes, U at a
-// time, and copying the input rows of the resident ones over their table
-// rows.  Result: the lane's own key's slot (or -1) and bucket.  `live`
-// selects the lanes whose key is probed.
-#ifndef HKV_ASSIGN_KEYS_PER_TILE
-#define HKV_ASSIGN_KEYS_PER_TILE 1
-#endif
-constexpr int kAssignKeysPerTile = HKV_ASSIGN_KEYS_PER_TILE;
-
-template <bool kPair, int U>
-__device__ __forceinline__ int warp_probe_update(const TableView& t, uint64_t k, uint64_t h,
-                                                uint64_t b1, uint64_t b2, bool live,
-                                                const float* values, uint64_t base, bool vec,
-                                                uint64_t& bkt) {
-  const unsigned lane = lane_id();
-  const unsigned sub = lane & 7u;
-  const unsigned tile0 = lane & 24u;
-  const unsigned tmask = 0xFFu << tile0;
-  const uint32_t my_pat = digest_of_hash(h) * 0x01010101u;
-  int my_slot = -1;
-  bkt = b1;
-#pragma unroll 1
-  for (int r = 0; r < 8; r += U) {
-    uint64_t kk[U], c1[U], c2[U];
-    uint32_t pat[U];
-    bool act[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int src = static_cast<int>(tile0) + r + u;
-      kk[u] = __shfl_sync(0xFFFFFFFFu, k, src);
-      c1[u] = __shfl_sync(0xFFFFFFFFu, b1, src);
-      c2[u] = kPair ? __shfl_sync(0xFFFFFFFFu, b2, src) : 0;
-      pat[u] = __shfl_sync(0xFFFFFFFFu, my_pat, src);
-      act[u] = __shfl_sync(0xFFFFFFFFu, live ? 1 : 0, src) != 0;
-    }
-    int slot[U];
-    uint64_t bk[U];
-    if (kPair) {
-      tile_probe_pair_many<U>(t, c1, c2, kk, pat, act, sub, tmask, slot, bk);
-    } else {
-      uint64_t unused[U];
-      tile_probe_many<U>(t, c1, kk, pat, act, sub, tmask, slot, unused);
-#pragma unroll
-      for (int u = 0; u < U; ++u) bk[u] = c1[u];
-    }
-    // resident keys: U row copies in flight
-    float* dst[U];
-    const float* src[U];
-    bool ok[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      ok[u] = slot[u] >= 0;
-      dst[u] = ok[u] ? row_ptr(t, bk[u] * kSlots + static_cast<uint64_t>(slot[u])) : nullptr;
-      src[u] = ok[u] ? values + (base + tile0 + r + u) * t.dim : values;
-    }
-    tile_copy_rows<U>(dst, src, ok, t.dim, sub, vec);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (sub == static_cast<unsigned>(r + u)) {
-        my_slot = slot[u];
-        bkt = bk[u];
-      }
-    }
-  }
-  return my_slot;
-}
-
 // Pass 1: resident keys update value (and score) in place; absent keys are
 // flagged in the dedup map (for the counts) and routed.
 #ifndef HKV_ASSIGN_MIN_BLOCKS
-#define HKV_ASSIGN_MIN_BLOCKS 6
+#define HKV_ASSIGN_MIN_BLOCKS 4
 #endif
 #ifndef HKV_ROUTE_MIN_BLOCKS
 #define HKV_ROUTE_MIN_BLOCKS 4
@@ -1641,43 +1498,101 @@ __device__ __forceinline__ int take_slot(uint4& m) {
   return -1;
 }
 
-// Candidate slots of the warp's probing keys in both of their buckets (HKV
-// §3.4: two fixed-length line loads per key): tile j loads the two digest
-// lines of each of keys 8j..8j+7, two keys' four lines in flight, and each
-// key's two 128-bit masks reach its lane through `msk` (32 keys x 16 x 16
-// bits: b1's line, then b2's).  Read-only loads: no thread of the route
-// kernel writes digests.
-__device__ __forceinline__ void route_candidates(const TableView& t, unsigned probe, uint32_t b1,
-                                                 uint32_t b2, uint32_t pat, unsigned lane,
-                                                 uint16_t (*msk)[16], uint4& c1, uint4& c2) {
+// Candidate slots of the warp's probing keys (HKV Algorithm 1; both
+// candidate buckets with kPair, HKV §3.4: two fixed-length line loads per
+// key): tile j loads the digest lines of keys 8j..8j+7, four lines in flight,
+// and each key's 128-bit masks reach its lane through `msk` (32 keys x 16 x
+// 16 bits: b1's line, then b2's).  Read-only loads: no thread of the calling
+// kernels writes digests.
+template <bool kPair>
+__device__ __forceinline__ void warp_candidates(const TableView& t, unsigned probe, uint32_t b1,
+                                                uint32_t b2, uint32_t pat, unsigned lane,
+                                                uint16_t (*msk)[16], uint4& c1, uint4& c2) {
   constexpr unsigned kFull = 0xFFFFFFFFu;
+  constexpr int KG = kPair ? 2 : 4;  // keys per group
   const unsigned tile = lane >> 3, sub = lane & 7u;
 #pragma unroll
-  for (int g = 0; g < 8; g += 2) {
-    uint4 d1[2], d2[2];
+  for (int g = 0; g < 8; g += KG) {
+    uint4 d1[KG], d2[KG];
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
+    for (int m = 0; m < KG; ++m) {
       const unsigned src = tile * 8 + g + m;
       const uint32_t x1 = __shfl_sync(kFull, b1, src);
-      const uint32_t x2 = __shfl_sync(kFull, b2, src);
+      const uint32_t x2 = kPair ? __shfl_sync(kFull, b2, src) : 0u;
       if ((probe >> src) & 1u) {
         d1[m] = ld_nc_v4(t.digests + static_cast<uint64_t>(x1) * kSlots + sub * 16);
-        d2[m] = ld_nc_v4(t.digests + static_cast<uint64_t>(x2) * kSlots + sub * 16);
+        if (kPair) d2[m] = ld_nc_v4(t.digests + static_cast<uint64_t>(x2) * kSlots + sub * 16);
       }
     }
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
+    for (int m = 0; m < KG; ++m) {
       const unsigned src = tile * 8 + g + m;
       const uint32_t p = __shfl_sync(kFull, pat, src);
       const bool on = (probe >> src) & 1u;
       msk[src][sub] = static_cast<uint16_t>(on ? digest_mask16(d1[m], p) : 0u);
-      msk[src][8 + sub] = static_cast<uint16_t>(on ? digest_mask16(d2[m], p) : 0u);
+      if (kPair) msk[src][8 + sub] = static_cast<uint16_t>(on ? digest_mask16(d2[m], p) : 0u);
     }
   }
   __syncwarp();
   c1 = *reinterpret_cast<const uint4*>(&msk[lane][0]);
-  c2 = *reinterpret_cast<const uint4*>(&msk[lane][8]);
+  c2 = kPair ? *reinterpret_cast<const uint4*>(&msk[lane][8]) : make_uint4(0, 0, 0, 0);
   __syncwarp();  // every lane has its masks before the next probe writes them
+}
+
+// The slot of the lane's key k (or -1) and the bucket holding it, from its
+// candidate masks: the first candidate of each bucket confirmed together,
+// then the rest (rare) in order; a key sits in at most one of its buckets.
+// Keys are read with read-only loads: no thread of the calling kernels
+// writes keys (the scores beside them are not read here).
+__device__ __forceinline__ int confirm_slot(const TableView& t, uint64_t k, uint32_t b1,
+                                            uint32_t b2, uint4 c1, uint4 c2, uint32_t& bk) {
+  bk = b1;
+  const int a1 = take_slot(c1), a2 = take_slot(c2);
+  uint64_t k1 = 0, k2 = 0;
+  if (a1 >= 0) k1 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + a1));
+  if (a2 >= 0) k2 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + a2));
+  if (a1 >= 0 && k1 == k) return a1;
+  if (a2 >= 0 && k2 == k) {
+    bk = b2;
+    return a2;
+  }
+  for (int c = take_slot(c1); c >= 0; c = take_slot(c1))
+    if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + c)) == k) return c;
+  for (int c = take_slot(c2); c >= 0; c = take_slot(c2)) {
+    if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + c)) == k) {
+      bk = b2;
+      return c;
+    }
+  }
+  return -1;
+}
+
+// Resident keys of the warp's 32 (slot >= 0): tile j copies the input rows
+// of keys 8j..8j+7 (batch indices base + 8j ..) over their table rows, two
+// rows in flight (more hold registers the calling kernels need).
+__device__ __forceinline__ void warp_copy_rows(const TableView& t, int slot, uint32_t bk,
+                                               const float* values, uint64_t base, bool vec,
+                                               unsigned lane) {
+  const unsigned tile = lane >> 3, sub = lane & 7u;
+  const unsigned tmask = 0xFFu << (tile * 8);
+  unsigned rows = (__ballot_sync(0xFFFFFFFFu, slot >= 0) >> (tile * 8)) & 0xFFu;
+  while (rows) {
+    float* dst[2];
+    const float* src[2];
+    bool ok[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      ok[r] = rows != 0;
+      const unsigned j = ok[r] ? __ffs(rows) - 1 : 0u;
+      if (ok[r]) rows &= rows - 1;
+      const unsigned from = tile * 8 + j;
+      const int s_ = __shfl_sync(tmask, slot, from);
+      const uint32_t b_ = __shfl_sync(tmask, bk, from);
+      dst[r] = ok[r] ? row_ptr(t, static_cast<uint64_t>(b_) * kSlots + s_) : nullptr;
+      src[r] = ok[r] ? values + (base + from) * t.dim : values;
+    }
+    tile_copy_rows<2>(dst, src, ok, t.dim, sub, vec);
+  }
 }
 
 // A warp takes 32 consecutive keys, one per lane for everything scalar (the
@@ -1694,8 +1609,6 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
   pdl_trigger();
   constexpr unsigned kFull = 0xFFFFFFFFu;
   const unsigned lane = lane_id();
-  const unsigned tile = lane >> 3, sub = lane & 7u;
-  const unsigned tmask = 0xFFu << (tile * 8);
   uint16_t(*msk)[16] = masks_sh[threadIdx.x >> 5];
   const uint64_t warps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   unsigned long long upd = 0, absent = 0;
@@ -1715,39 +1628,9 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
     const unsigned probe = __ballot_sync(kFull, live);
     if (!probe) continue;
     uint4 c1, c2;
-    route_candidates(t, probe, b1, b2, digest_of_hash(h) * 0x01010101u, lane, msk, c1, c2);
-    // confirm: the first candidate of each bucket in flight together, then
-    // the rest (rare) in order; a key sits in at most one of its buckets
-    int slot = -1;
+    warp_candidates<true>(t, probe, b1, b2, digest_of_hash(h) * 0x01010101u, lane, msk, c1, c2);
     uint32_t bk = b1;
-    if (live) {
-      const int a1 = take_slot(c1), a2 = take_slot(c2);
-      uint64_t k1 = 0, k2 = 0;
-      if (a1 >= 0) k1 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + a1));
-      if (a2 >= 0) k2 = ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + a2));
-      if (a1 >= 0 && k1 == k) {
-        slot = a1;
-      } else if (a2 >= 0 && k2 == k) {
-        slot = a2;
-        bk = b2;
-      } else {
-        for (int c = take_slot(c1); c >= 0; c = take_slot(c1)) {
-          if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b1) * kSlots + c)) == k) {
-            slot = c;
-            break;
-          }
-        }
-        if (slot < 0) {
-          for (int c = take_slot(c2); c >= 0; c = take_slot(c2)) {
-            if (ld_nc_u64(key_at(t, static_cast<uint64_t>(b2) * kSlots + c)) == k) {
-              slot = c;
-              bk = b2;
-              break;
-            }
-          }
-        }
-      }
-    }
+    const int slot = live ? confirm_slot(t, k, b1, b2, c1, c2, bk) : -1;
     if (live) {
       sc.absent[ms] = slot < 0 ? 1 : 0;  // read by the second bucket pass
       const uint64_t inc = entry_inc(sc, ms);
@@ -1761,27 +1644,7 @@ __global__ void __launch_bounds__(kThreads, HKV_ROUTE_MIN_BLOCKS) dual_route_ker
         if (target != kNoBucket) stage_routed(t, sc, target, k, h, i, inc);
       }
     }
-    // resident keys: tile j copies the input rows of keys 8j..8j+7 over
-    // their table rows, two rows in flight (more hold registers the
-    // rest of the kernel needs)
-    unsigned rows = (__ballot_sync(kFull, slot >= 0) >> (tile * 8)) & 0xFFu;
-    while (rows) {
-      float* dst[2];
-      const float* src[2];
-      bool ok[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        ok[r] = rows != 0;
-        const unsigned j = ok[r] ? __ffs(rows) - 1 : 0u;
-        if (ok[r]) rows &= rows - 1;
-        const unsigned from = tile * 8 + j;
-        const int s_ = __shfl_sync(tmask, slot, from);
-        const uint32_t b_ = __shfl_sync(tmask, bk, from);
-        dst[r] = ok[r] ? row_ptr(t, static_cast<uint64_t>(b_) * kSlots + s_) : nullptr;
-        src[r] = ok[r] ? values + (base + from) * t.dim : values;
-      }
-      tile_copy_rows<2>(dst, src, ok, t.dim, sub, vec);
-    }
+    warp_copy_rows(t, slot, bk, values, base, vec, lane);
   }
   warp_add(&t.stats->updated, upd);
   // the call's absent keys; dual_finish_kernel splits them into admitted
@@ -1833,7 +1696,10 @@ template <bool kDual>
 __global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel(
     TableView t, UpsertScratch sc, uint64_t n, const uint64_t* keys, const float* values,
     ScoreRule rule, bool keep_scores, bool vec) {
+  __shared__ __align__(16) uint16_t masks_sh[kThreads / 32][32][16];
+  constexpr unsigned kFull = 0xFFFFFFFFu;
   const unsigned lane = lane_id();
+  uint16_t(*msk)[16] = masks_sh[threadIdx.x >> 5];
   const uint64_t warps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   unsigned long long upd = 0;
   for (uint64_t base = ((static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 32;
@@ -1843,16 +1709,22 @@ __global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel
     const uint32_t ms = i < n && !is_reserved(k) ? map_last_occurrence(sc, k, i) : kNone;
     const bool live = ms != kNone;  // the key's last occurrence in the batch
     const uint64_t h = hash64(k);
-    const uint64_t b1 = bucket_of_hash(t, h);
-    uint64_t b;
-    const int slot = warp_probe_update<kDual, kAssignKeysPerTile>(
-        t, k, h, b1, kDual ? bucket2_of(t, k, b1) : b1, live, values, base, vec, b);
-    if (!live || slot < 0) continue;
-    if (!keep_scores) {
-      uint64_t* sp = score_at(t, b * kSlots + static_cast<uint64_t>(slot));
-      *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
+    const uint32_t b1 = static_cast<uint32_t>(bucket_of_hash(t, h));
+    const uint32_t b2 = kDual ? static_cast<uint32_t>(bucket2_of(t, k, b1)) : b1;
+    const unsigned probe = __ballot_sync(kFull, live);
+    if (!probe) continue;
+    uint4 c1, c2;
+    warp_candidates<kDual>(t, probe, b1, b2, digest_of_hash(h) * 0x01010101u, lane, msk, c1, c2);
+    uint32_t bk = b1;
+    const int slot = live ? confirm_slot(t, k, b1, b2, c1, c2, bk) : -1;
+    if (slot >= 0) {
+      if (!keep_scores) {
+        uint64_t* sp = score_at(t, static_cast<uint64_t>(bk) * kSlots + static_cast<uint64_t>(slot));
+        *sp = policy_score(rule, i, entry_inc(sc, ms), true, rule.lfu() ? *sp : 0ull);
+      }
+      ++upd;
     }
-    ++upd;
+    warp_copy_rows(t, slot, bk, values, base, vec, lane);
   }
   warp_add(&t.stats->updated, upd);
 }
