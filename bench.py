@@ -155,16 +155,29 @@ def probe_access_rates(granules):
     return out
 
 
-def probe_host_link(row_bytes):
-    """SM loads and stores over mapped pinned host memory (the path tiered
-    rows take): streaming and random rows of `row_bytes`, bytes per second."""
+HOST_SLAB_MAPPED_MAX = 16 << 30  # HKV_HOST_SLAB_MAPPED_MAX of include/hkv.h
+
+
+def slab_kinds(slab_bytes):
+    """The probe kinds (random row reads, writes) over the memory a tiered
+    table allocates for a host slab of `slab_bytes`: mapped memory up to
+    HOST_SLAB_MAPPED_MAX, a host-NUMA pool above."""
+    return (2, 3) if slab_bytes <= HOST_SLAB_MAPPED_MAX else (6, 7)
+
+
+def probe_host_link(row_bytes, buffer_bytes=1 << 30, kinds=(0, 1, 2, 3)):
+    """SM loads and stores over pinned host memory allocated as a tiered
+    table's slab is (the path tiered rows take): streaming and random rows of
+    `row_bytes` over a buffer of `buffer_bytes`, bytes per second."""
     import ctypes
     lib = _probe_lib()
+    names = {0: "stream_read", 1: "stream_write", 2: "row_read", 3: "row_write",
+             6: "row_read", 7: "row_write"}  # 4 + kind: pool memory
     out = {}
-    for kind, name in ((0, "stream_read"), (1, "stream_write"), (2, "row_read"), (3, "row_write")):
+    for kind in kinds:
         r = ctypes.c_double(0.0)
-        st = lib.hkv_probe_host_link(kind, row_bytes, 1 << 30, ctypes.byref(r))
-        out[name] = r.value if st == 0 else None
+        st = lib.hkv_probe_host_link(kind, row_bytes, buffer_bytes, ctypes.byref(r))
+        out[names[kind]] = r.value if st == 0 else None
     return out
 
 
@@ -243,10 +256,10 @@ def rows_of_ptrs(ptrs, found, info):
 # dram__bytes_read.sum,dram__bytes_write.sum --clock-control none.
 # ---------------------------------------------------------------------------
 NCU_TRAFFIC = {
-    "find_kernel": {"bytes": 269862571, "sources": ("find.cu", "common.cuh", "launch.h"),
-                    "sha256": "5601ef67d0d10579"},
-    "upsert_single_kernel": {"bytes": 330487381, "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "9db1a3830a3e621f"},
+    "find_kernel": {"bytes": 269957291, "sources": ("find.cu", "common.cuh", "launch.h"),
+                    "sha256": "4dee867c0f4192e6"},
+    "upsert_single_kernel": {"bytes": 330717525, "sources": ("upsert.cu", "common.cuh", "launch.h"),
+                             "sha256": "379ddb92f7c50d69"},
 }
 
 
@@ -853,12 +866,15 @@ def cfg_c4(ctx, steps, warmup, peak, small=False):
             "steps": steps}
 
 
-def cfg_c5(ctx, steps, warmup, peak, link):
+def cfg_c5(ctx, steps, warmup, peak, link, link_slab=None):
     """Tiered mixed stream: find, assign and insert_or_assign batches on
     three streams (3:1:1), ordered by the table's roles.  Link bound: the
     value bytes that cross the host link (rows of host-resident keys read by
     finds and written by assign / insert_or_assign) at the probed SM-access
-    rates, against the HBM bytes at the copy peak."""
+    rates, against the HBM bytes at the copy peak.  `link`: random rows over
+    a 1 GiB buffer (the link itself); `link_slab`: over a buffer the size of
+    the table's 32 GiB slab, where the device's address translation of host
+    memory, not the link, sets the rate of random rows."""
     torch, hkv = ctx.torch, ctx.hkv
     cap, dim, n = 1 << 28, 64, 1 << 20
     rb = 4 * dim
@@ -927,13 +943,22 @@ def cfg_c5(ctx, steps, warmup, peak, link):
     link_s = (rd_b / link["row_read"] + wr_b / link["row_write"]) if link.get("row_read") else None
     hbm_s = hb / (peak * 1e9)
     bound = max(x for x in (link_s, hbm_s) if x is not None)
-    return {"value": 5 * n / step / 1e9, "ms_per_step": step * 1e3,
-            "host_read_bytes_per_step": rd_b, "host_write_bytes_per_step": wr_b,
-            "hbm_bytes_per_step": hb, "link_bound_s": link_s, "hbm_bound_s": hbm_s,
-            "frac_of_bound": bound / step,
-            "bound": "host link" if link_s and link_s >= hbm_s else "hbm",
-            "link": "SM loads/stores over mapped pinned host memory (NVLink-C2C on a Grace host)",
-            "steps": steps, "gpu_launches_per_step": 9}
+    out = {"value": 5 * n / step / 1e9, "ms_per_step": step * 1e3,
+           "host_read_bytes_per_step": rd_b, "host_write_bytes_per_step": wr_b,
+           "hbm_bytes_per_step": hb, "link_bound_s": link_s, "hbm_bound_s": hbm_s,
+           "frac_of_bound": bound / step,
+           "bound": "host link" if link_s and link_s >= hbm_s else "hbm",
+           "link": "SM loads/stores over pinned host memory (a host-NUMA memory pool; "
+                   "NVLink-C2C on a Grace host)",
+           "steps": steps, "gpu_launches_per_step": 9}
+    if link_slab and link_slab.get("row_read") and link_slab.get("row_write"):
+        slab_s = rd_b / link_slab["row_read"] + wr_b / link_slab["row_write"]
+        # uniform random rows over a slab this size: the skewed stream's hot
+        # rows stay in L2, so this is context for the slab's memory, not a
+        # bound on the step
+        out["slab_uniform_row_rates_bytes_per_s"] = link_slab
+        out["slab_uniform_rows_s"] = slab_s
+    return out
 
 
 def run_gpu(args):
@@ -1004,13 +1029,16 @@ def run_gpu(args):
         link = {}
         try:
             link = probe_host_link(4 * 64)
+            link_slab = probe_host_link(4 * 64, 32 << 30, kinds=slab_kinds(32 << 30))
         except Exception as exc:
-            link = {"unavailable": str(exc)}
+            link, link_slab = {"unavailable": str(exc)}, {}
         configs["host_link_bytes_per_s"] = link
+        configs["host_link_bytes_per_s_32GiB"] = link_slab
         for name, fn in (("c1", lambda: cfg_c1(ctx, 5, 3, peak)),
                          ("c3", lambda: cfg_c3(ctx, args.config_steps, 3, peak)),
                          ("c4", lambda: cfg_c4(ctx, args.config_steps, 3, peak)),
-                         ("c5", lambda: cfg_c5(ctx, min(args.config_steps, 3), 2, peak, link))):
+                         ("c5", lambda: cfg_c5(ctx, min(args.config_steps, 3), 2, peak, link,
+                                              link_slab))):
             try:
                 configs[name] = {"workload": OTHER[name], **fn()}
             except Exception as exc:
@@ -1069,7 +1097,8 @@ def run_other(args):
     elif cfg == "c4":
         r = cfg_c4(ctx, args.steps, args.warmup, peak, small=args.small)
     else:
-        r = cfg_c5(ctx, args.steps, args.warmup, peak, probe_host_link(4 * 64))
+        r = cfg_c5(ctx, args.steps, args.warmup, peak, probe_host_link(4 * 64),
+                   probe_host_link(4 * 64, 32 << 30, kinds=slab_kinds(32 << 30)))
     line = {
         "metric": METRIC, "value": r["value"], "unit": "B-KV/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r.get("ms_per_step"),
@@ -1280,8 +1309,9 @@ def run_ablation(args):
 
 def run_probe_sweep():
     """Random reads of 32..512-byte granules over a 4 GiB buffer at 1..16
-    reads in flight and 2, 4, 8 blocks per SM (G reads/s), and the host link
-    by SM loads and stores (GB/s)."""
+    reads in flight and 2, 4, 8 blocks per SM (G reads/s), the host link by
+    SM loads and stores (GB/s), and random host rows by buffer size and
+    memory kind (GB/s)."""
     import ctypes
 
     import torch
@@ -1297,7 +1327,17 @@ def run_probe_sweep():
                 st = lib.hkv_probe_random_reads_at(g, 4 << 30, d, b, ctypes.byref(r))
                 grid[f"{g}B blocks={b} depth={d}"] = round(r.value / 1e9, 2) if st == 0 else None
     link = {k: (round(v / 1e9, 1) if v else None) for k, v in probe_host_link(256).items()}
-    print(json.dumps({"random_reads_G_per_s": grid, "host_link_GB_per_s": link}))
+    # random 256-byte rows over host buffers of growing size, mapped memory
+    # and host-NUMA pool memory (the two kinds a tiered slab can be)
+    slab = {}
+    for gib in (1, 8, 16, 17, 18, 20, 24, 32):
+        for kinds, name in (((2, 3), "mapped"), ((6, 7), "pool")):
+            if name == "pool" and gib not in (1, 8, 16, 32):
+                continue
+            r = probe_host_link(256, gib << 30, kinds=kinds)
+            slab[f"{name} {gib} GiB"] = {k: (round(v / 1e9, 1) if v else None) for k, v in r.items()}
+    print(json.dumps({"random_reads_G_per_s": grid, "host_link_GB_per_s": link,
+                      "host_rows_by_buffer_size_GB_per_s": slab}))
 
 
 def main():

@@ -107,14 +107,26 @@ cudaError_t launch_depth(int depth, uint32_t granule, const uint8_t* buf, uint64
   }
 }
 
-// Host-link probe kernels: 16-byte SM loads / stores over mapped host memory.
-// Streaming: the grid walks the buffer in consecutive 16-byte vectors.
+// Host-link probe kernels: 16-byte SM loads / stores over host memory, with
+// the instructions the table's kernels use for rows of the host slab (plain
+// loads, streaming stores; loads through the read-only path reach half the
+// rate).  Streaming: the grid walks the buffer in consecutive 16-byte vectors.
+__device__ __forceinline__ uint4 ld_row_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_row_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __global__ void host_stream_read(const uint4* p, uint64_t nvec, unsigned long long* sink) {
   uint32_t acc = 0;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < nvec;
        i += stride) {
-    const uint4 w = __ldcg(p + i);
+    const uint4 w = ld_row_v4(p + i);
     acc ^= w.x ^ w.w;
   }
   if (acc == 0x5EEDu) *sink = acc;
@@ -124,12 +136,13 @@ __global__ void host_stream_write(uint4* p, uint64_t nvec) {
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < nvec;
        i += stride)
-    p[i] = make_uint4(static_cast<uint32_t>(i), 1u, 2u, 3u);
+    st_row_v4(p + i, make_uint4(static_cast<uint32_t>(i), 1u, 2u, 3u));
 }
 
 // Random rows of `granule` bytes (a multiple of 16, at most 512), one row per
-// 8-lane tile at a time, 4 rows in flight per tile; `rows` is a power of two.
-__global__ void host_row_read(const uint8_t* p, uint64_t row_mask, uint32_t granule,
+// 8-lane tile at a time, 4 rows in flight per tile; row indices uniform in
+// [0, rows) (the high half of a 64x64-bit product, always below rows).
+__global__ void host_row_read(const uint8_t* p, uint64_t rows, uint32_t granule,
                               uint32_t iters, unsigned long long* sink) {
   const uint64_t tile = (blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x) >> 3;
   const uint32_t sub = threadIdx.x & 7u;
@@ -139,12 +152,11 @@ __global__ void host_row_read(const uint8_t* p, uint64_t row_mask, uint32_t gran
     uint4 v[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it * 4 + u) & row_mask;
+      const uint64_t g = __umul64hi(mix64(tile * 0xD1B54A32D192ED03ull + it * 4 + u), rows);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint32_t q = sub + 8u * c;
-        v[u][c] = q < vecs ? __ldcg(reinterpret_cast<const uint4*>(p + g * granule + 16 * q))
-                           : make_uint4(0, 0, 0, 0);
+        v[u][c] = q < vecs ? ld_row_v4(p + g * granule + 16 * q) : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
@@ -155,14 +167,14 @@ __global__ void host_row_read(const uint8_t* p, uint64_t row_mask, uint32_t gran
   if (acc == 0x5EEDu) *sink = acc;
 }
 
-__global__ void host_row_write(uint8_t* p, uint64_t row_mask, uint32_t granule, uint32_t iters) {
+__global__ void host_row_write(uint8_t* p, uint64_t rows, uint32_t granule, uint32_t iters) {
   const uint64_t tile = (blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x) >> 3;
   const uint32_t sub = threadIdx.x & 7u;
   const uint32_t vecs = granule / 16;
   for (uint32_t it = 0; it < iters; ++it) {
-    const uint64_t g = mix64(tile * 0xD1B54A32D192ED03ull + it) & row_mask;
+    const uint64_t g = __umul64hi(mix64(tile * 0xD1B54A32D192ED03ull + it), rows);
     for (uint32_t q = sub; q < vecs; q += 8)
-      *reinterpret_cast<uint4*>(p + g * granule + 16 * q) = make_uint4(it, 1u, 2u, 3u);
+      st_row_v4(p + g * granule + 16 * q, make_uint4(it, 1u, 2u, 3u));
   }
 }
 
@@ -244,38 +256,80 @@ int hkv_probe_random_reads(uint32_t granule, uint64_t buffer_bytes, double* read
   return hkv_probe_random_reads_at(granule, p, 4, 8, reads_per_s);
 }
 
-// Measures SM access to mapped pinned host memory, the path tiered mode's
-// value rows take.  kind: 0 = streaming 16-byte reads, 1 = streaming 16-byte
+// Pinned host memory the device reads and writes at the same address, drawn
+// from a memory pool on the host NUMA node nearest the device, as a tiered
+// table's value slab is.
+static cudaError_t pool_host_buffer(int dev, uint64_t bytes, cudaMemPool_t* pool, void** p) {
+  int numa = -1;
+  if (cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, dev) != cudaSuccess) {
+    cudaGetLastError();
+    numa = -1;
+  }
+  cudaMemPoolProps props{};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = numa >= 0 ? cudaMemLocationTypeHostNuma : cudaMemLocationTypeHost;
+  props.location.id = numa >= 0 ? numa : 0;
+  cudaError_t e = cudaMemPoolCreate(pool, &props);
+  if (e != cudaSuccess) {
+    *pool = nullptr;
+    return e;
+  }
+  cudaMemAccessDesc access{};
+  access.location.type = cudaMemLocationTypeDevice;
+  access.location.id = dev;
+  access.flags = cudaMemAccessFlagsProtReadWrite;
+  e = cudaMemPoolSetAccess(*pool, &access, 1);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(p, bytes, *pool, cudaStreamLegacy);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
+  return e;
+}
+
+// Measures SM access to pinned host memory, the path tiered mode's value
+// rows take.  kind & 3: 0 = streaming 16-byte reads, 1 = streaming 16-byte
 // writes, 2 = random reads of `granule`-byte rows, 3 = random writes of
-// `granule`-byte rows (granule a multiple of 16, 16..512).  `buffer_bytes` is
-// a power of two of at least 64 MiB; the host buffer is allocated with
-// cudaHostAllocMapped and freed before return.  Writes bytes per second to
-// *bytes_per_s.  Returns 0, -1 on bad arguments, or the CUDA error code.
-// Synchronises the device.
+// `granule`-byte rows (granule a multiple of 16, 16..512).  kind & 4: the
+// buffer comes from a host-NUMA memory pool (as a tiered slab above
+// HKV_HOST_SLAB_MAPPED_MAX does), else from cudaHostAllocMapped.
+// `buffer_bytes` is a multiple of 64 MiB; the buffer is freed
+// before return.  Writes to *bytes_per_s the best rate over 4, 8 and 16
+// blocks of 256 threads per SM (each launch moves about buffer_bytes, at
+// most 4 GiB for the random kinds; one untimed launch first).  Returns 0, -1
+// on bad arguments, or the CUDA error code.  Synchronises the device.
 int hkv_probe_host_link(int kind, uint32_t granule, uint64_t buffer_bytes, double* bytes_per_s) {
-  if (!bytes_per_s || kind < 0 || kind > 3 || !pow2(buffer_bytes) || buffer_bytes < (64ull << 20))
+  if (!bytes_per_s || kind < 0 || kind > 7 || buffer_bytes == 0 ||
+      buffer_bytes % (64ull << 20) != 0)
     return -1;
+  const bool pooled = (kind & 4) != 0;
+  kind &= 3;
   if (kind >= 2 && (granule % 16 != 0 || granule < 16 || granule > 512)) return -1;
+  cudaMemPool_t pool = nullptr;
   void* host = nullptr;
   uint8_t* dp = nullptr;
   unsigned long long* sink = nullptr;
-  cudaError_t e = cudaHostAlloc(&host, buffer_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dp), host, 0);
-  if (e == cudaSuccess) e = cudaMalloc(&sink, sizeof(unsigned long long));
   int dev = 0, sms = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) {
+    if (pooled) {
+      e = pool_host_buffer(dev, buffer_bytes, &pool, reinterpret_cast<void**>(&dp));
+    } else {
+      e = cudaHostAlloc(&host, buffer_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+      if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dp), host, 0);
+    }
+  }
+  if (e == cudaSuccess) e = cudaMalloc(&sink, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   Timer tm;
   if (e == cudaSuccess) e = tm.init();
-  if (e == cudaSuccess) {
-    const unsigned grid = static_cast<unsigned>(sms) * 4;
-    const uint64_t nvec = buffer_bytes / 16;
-    uint64_t rows = 1;
-    if (kind >= 2)
-      while (rows * 2 * granule <= buffer_bytes) rows *= 2;
+  double best = 0.0;
+  const uint64_t nvec = buffer_bytes / 16;
+  const uint64_t rows = buffer_bytes / granule;  // whole rows of the buffer
+  for (int per_sm = 4; e == cudaSuccess && per_sm <= 16; per_sm *= 2) {
+    const unsigned grid = static_cast<unsigned>(sms) * per_sm;
     const uint64_t tiles = static_cast<uint64_t>(grid) * 256 / 8;
-    // random kinds: about buffer_bytes of rows per launch
-    uint32_t iters = kind >= 2 ? static_cast<uint32_t>(buffer_bytes / granule / tiles) : 0;
+    // random kinds: rows drawn from the whole buffer, about min(buffer_bytes,
+    // 4 GiB) of them per launch
+    const uint64_t moved = buffer_bytes < (4ull << 30) ? buffer_bytes : (4ull << 30);
+    uint32_t iters = kind >= 2 ? static_cast<uint32_t>(moved / granule / tiles) : 0;
     if (kind == 2) iters = (iters + 3) / 4;  // 4 rows per iteration
     if (kind >= 2 && iters < 1) iters = 1;
     double bytes = 0;
@@ -285,9 +339,9 @@ int hkv_probe_host_link(int kind, uint32_t granule, uint64_t buffer_bytes, doubl
                 bytes = static_cast<double>(buffer_bytes); break;
         case 1: host_stream_write<<<grid, 256>>>(reinterpret_cast<uint4*>(dp), nvec);
                 bytes = static_cast<double>(buffer_bytes); break;
-        case 2: host_row_read<<<grid, 256>>>(dp, rows - 1, granule, iters, sink);
+        case 2: host_row_read<<<grid, 256>>>(dp, rows, granule, iters, sink);
                 bytes = static_cast<double>(tiles) * iters * 4 * granule; break;
-        default: host_row_write<<<grid, 256>>>(dp, rows - 1, granule, iters);
+        default: host_row_write<<<grid, 256>>>(dp, rows, granule, iters);
                  bytes = static_cast<double>(tiles) * iters * granule; break;
       }
       return cudaGetLastError();
@@ -299,10 +353,16 @@ int hkv_probe_host_link(int kind, uint32_t granule, uint64_t buffer_bytes, doubl
     if (e == cudaSuccess) e = cudaEventSynchronize(tm.b);
     float ms = 0.f;
     if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, tm.a, tm.b);
-    if (e == cudaSuccess) *bytes_per_s = ms > 0.f ? bytes / (ms * 1e-3) : 0.0;
+    if (e == cudaSuccess && ms > 0.f && bytes / (ms * 1e-3) > best) best = bytes / (ms * 1e-3);
   }
+  if (e == cudaSuccess) *bytes_per_s = best;
   if (sink) cudaFree(sink);
+  cudaDeviceSynchronize();
   if (host) cudaFreeHost(host);
+  if (pool) {
+    if (dp) cudaFree(dp);
+    cudaMemPoolDestroy(pool);
+  }
   return e == cudaSuccess ? 0 : static_cast<int>(e);
 }
 

@@ -175,6 +175,17 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 // Streaming store (evict-first), for output rows and written value rows.
+// A value row in the host slab of a tiered table is read with a plain
+// (L1-cached) load: on a GB300 over NVLink-C2C, SM reads of host memory
+// through the read-only path, with or without L1 allocation, reach half of
+// the link's rate (105.6 GB/s for random 256-byte rows), plain loads the
+// whole of it (211.1 GB/s).  HBM rows keep ld_stream_v4.
+__device__ __forceinline__ uint4 ld_host_row_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
 __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -303,11 +314,12 @@ __device__ __forceinline__ void warp_add(unsigned long long* p, unsigned long lo
 // (0..7) moves 16-byte chunks sub, sub+8, ...  `vec` selects the 16-byte path
 // (both rows 16-byte aligned and dim % 4 == 0); otherwise 4-byte words.
 __device__ __forceinline__ void tile_copy_row(float* dst, const float* src, uint32_t dim,
-                                              unsigned sub, bool vec, bool stream_store) {
+                                              unsigned sub, bool vec, bool stream_store,
+                                              bool src_host = false) {
   if (vec) {
     const uint32_t chunks = dim >> 2;
     for (uint32_t c = sub; c < chunks; c += 8) {
-      uint4 v = ld_stream_v4(src + 4 * c);
+      uint4 v = src_host ? ld_host_row_v4(src + 4 * c) : ld_stream_v4(src + 4 * c);
       if (stream_store) st_stream_v4(dst + 4 * c, v);
       else *reinterpret_cast<uint4*>(dst + 4 * c) = v;
     }

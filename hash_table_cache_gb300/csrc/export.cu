@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(kThreads) export_kernel(TableView t, uint64_t 
     }
     pos = __shfl_sync(tmask, pos, lane & 24u);
     if (values_out)
-      tile_copy_row(values_out + pos * t.dim, row_ptr(t, row), t.dim, sub, vec, true);
+      tile_copy_row(values_out + pos * t.dim, row_ptr(t, row), t.dim, sub, vec, true,
+                    row >= t.hbm_rows);
   }
 }
 

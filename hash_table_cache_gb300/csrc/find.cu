@@ -255,9 +255,10 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
         const unsigned src = tile * 8 + m;
         const int s = __shfl_sync(kFull, slot, src);
         const uint32_t b = __shfl_sync(kFull, bkt, src);
+        const uint64_t row = static_cast<uint64_t>(b) * kSlots + s;
         if ((hits >> src) & 1u)
-          tile_copy_row(values_out + static_cast<uint64_t>(base + src) * t.dim,
-                        row_ptr(t, static_cast<uint64_t>(b) * kSlots + s), t.dim, sub, vec, true);
+          tile_copy_row(values_out + static_cast<uint64_t>(base + src) * t.dim, row_ptr(t, row),
+                        t.dim, sub, vec, true, row >= t.hbm_rows);
       }
       continue;
     }
@@ -272,11 +273,13 @@ __global__ void __launch_bounds__(256, HKV_FIND_MIN_BLOCKS)
         const int s = __shfl_sync(kFull, slot, src);
         const uint32_t b = __shfl_sync(kFull, bkt, src);
         if ((hits >> src) & 1u) {
-          const float* p = row_ptr(t, static_cast<uint64_t>(b) * kSlots + s);
+          const uint64_t row = static_cast<uint64_t>(b) * kSlots + s;
+          const float* p = row_ptr(t, row);
+          const bool host = row >= t.hbm_rows;  // a row of the tiered host slab
 #pragma unroll
           for (int c = 0; c < C; ++c) {
             const uint32_t q = sub + 8u * c;
-            if (q < chunks) v[r][c] = ld_stream_v4(p + 4 * q);
+            if (q < chunks) v[r][c] = host ? ld_host_row_v4(p + 4 * q) : ld_stream_v4(p + 4 * q);
           }
         }
       }

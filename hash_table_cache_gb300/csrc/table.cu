@@ -144,7 +144,8 @@ struct hkv_table {
   int device = 0;
   uint32_t mode = 0;
   uint64_t capacity = 0;
-  float* host_slab = nullptr;  // host address of the mapped value slab
+  void* host_slab = nullptr;  // the tiered value slab as allocated (values_host: its device address)
+  cudaMemPool_t host_pool = nullptr;  // its pool, for slabs above HKV_HOST_SLAB_MAPPED_MAX
   cudaMemPool_t pool = nullptr;
   cudaStream_t aux = nullptr;
   uint64_t step = 1;       // step counter / clock of the score policies
@@ -168,11 +169,59 @@ void release(hkv_table* t) {
   cudaFree(t->v.values_hbm);
   cudaFree(t->v.summary);
   cudaFree(t->v.stats);
-  if (t->host_slab) cudaFreeHost(t->host_slab);
+  // the table's work has finished (wait_all above): the slab is unused
+  if (t->host_pool) {
+    if (t->host_slab) cudaFree(t->host_slab);
+    cudaMemPoolDestroy(t->host_pool);
+  } else if (t->host_slab) {
+    cudaFreeHost(t->host_slab);
+  }
   delete t;
 }
 
 bool batch_ok(hkv_table* t, uint64_t n) { return t && n <= HKV_MAX_BATCH; }
+
+// The tiered value slab, pinned host memory the device reads and writes at
+// the same address.  Up to HKV_HOST_SLAB_MAPPED_MAX bytes it is
+// cudaHostAllocMapped memory; a larger slab comes from a memory pool on the
+// host NUMA node nearest the device (the host location where the system has
+// no NUMA ids).  The two differ in how the device reaches random rows: mapped
+// memory reads fastest while the process's mapped footprint stays small, and
+// falls steeply past it; pool memory reads more slowly but holds its rate at
+// any size (figures in include/hkv.h).
+cudaError_t alloc_host_slab(int device, size_t bytes, cudaMemPool_t* pool, void** host,
+                            void** slab) {
+  *pool = nullptr;
+  *host = nullptr;
+  if (bytes <= HKV_HOST_SLAB_MAPPED_MAX) {
+    cudaError_t e = cudaHostAlloc(host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(slab, *host, 0);
+    return e;
+  }
+  int numa = -1;
+  if (cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, device) != cudaSuccess) {
+    cudaGetLastError();
+    numa = -1;
+  }
+  cudaMemPoolProps props{};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = numa >= 0 ? cudaMemLocationTypeHostNuma : cudaMemLocationTypeHost;
+  props.location.id = numa >= 0 ? numa : 0;
+  cudaError_t e = cudaMemPoolCreate(pool, &props);
+  if (e != cudaSuccess) {
+    *pool = nullptr;
+    return e;
+  }
+  cudaMemAccessDesc access{};
+  access.location.type = cudaMemLocationTypeDevice;
+  access.location.id = device;
+  access.flags = cudaMemAccessFlagsProtReadWrite;
+  e = cudaMemPoolSetAccess(*pool, &access, 1);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(slab, bytes, *pool, cudaStreamLegacy);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
+  if (e == cudaSuccess) *host = *slab;
+  return e;
+}
 
 bool clock_policy(const hkv_table* t) {
   return t->policy == hkv::kLru || t->policy == hkv::kEpochLru;
@@ -302,10 +351,8 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
   if (e == cudaSuccess && hbm_rows) e = cudaMalloc(&v.values_hbm, hbm_rows * 4ull * dim);
   if (e == cudaSuccess && dual) e = cudaMalloc(&v.summary, nb * sizeof(hkv::BucketSummary));
   if (e == cudaSuccess && hbm_rows < capacity) {
-    e = cudaHostAlloc(reinterpret_cast<void**>(&t->host_slab), (capacity - hbm_rows) * 4ull * dim,
-                      cudaHostAllocMapped | cudaHostAllocPortable);
-    if (e == cudaSuccess)
-      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&v.values_host), t->host_slab, 0);
+    e = alloc_host_slab(device, (capacity - hbm_rows) * 4ull * dim, &t->host_pool, &t->host_slab,
+                        reinterpret_cast<void**>(&v.values_host));
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&t->aux, cudaStreamNonBlocking);
   // role events for the first calls (a call reuses the events of the calls

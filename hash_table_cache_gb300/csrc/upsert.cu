@@ -781,7 +781,8 @@ __global__ void __launch_bounds__(kBucketThreads, HKV_UPSERT_MIN_BLOCKS) upsert_
                                    ? values_in + static_cast<uint64_t>(src_i) * t.dim
                                    : row_ptr(t, b * kSlots + st.ev_slot[j]);
             tile_copy_row(ex.ev_values + static_cast<uint64_t>(st.ev_o[j]) * t.dim, src, t.dim,
-                          sub, evec, true);
+                          sub, evec, true,
+                          src_i == kNone && b * kSlots + st.ev_slot[j] >= t.hbm_rows);
           }
         }
         __syncwarp();

@@ -127,7 +127,8 @@ enum {
  *                  | one HKV_POLICY_* (default HKV_POLICY_CUSTOMIZED).
  *  value_hbm_bytes with TIERED: HBM budget for value rows.  Rows of whole
  *                  buckets 0 .. R-1 (R = floor(budget / (128 * 4 * dim)) * 128)
- *                  live in HBM, the rest in mapped pinned host memory.
+ *                  live in HBM, the rest in pinned host memory the device
+ *                  reads and writes directly (see HKV_HOST_SLAB_MAPPED_MAX).
  *                  Ignored without TIERED (all rows in HBM).
  *  device          CUDA device ordinal the table lives on.
  *  out             receives the table handle.
@@ -135,6 +136,16 @@ enum {
  * Synchronous.  Errors: INVALID, OOM, CUDA (nothing is leaked). */
 hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t value_hbm_bytes,
                       int device, hkv_table** out);
+
+/* The host slab of a tiered table (the rows above the HBM budget) is
+ * cudaHostAllocMapped memory when it holds at most this many bytes, and
+ * pinned memory from a memory pool on the device's nearest host NUMA node
+ * when it is larger.  Measured on a GB300 (Grace host, 64 KiB pages, NVLink-
+ * C2C), random 256-byte row reads from the GPU: mapped memory reads at 183-208
+ * GB/s while the process's mapped footprint is at most 16 GiB and at 7-12
+ * GB/s beyond 24 GiB; pool memory reads at 26-28 GB/s from 8 GiB to 32 GiB.
+ * Either way a row's device address is fixed for the table's life. */
+#define HKV_HOST_SLAB_MAPPED_MAX (16ull << 30)
 
 /* Wait for all work on the table and free it.  NULL is a no-op. */
 hkv_status hkv_destroy(hkv_table* table);

@@ -133,3 +133,14 @@ def test_ncu_traffic_follows_sources(monkeypatch):
     monkeypatch.setitem(bench.NCU_TRAFFIC, "probe_kernel", stale)
     assert bench.ncu_traffic("probe_kernel") is None
     assert bench.ncu_traffic("no_such_kernel") is None
+
+
+def test_slab_threshold_matches_the_header():
+    """The bench probes a tiered slab's memory the way the library allocates
+    it: the size threshold is the header's HKV_HOST_SLAB_MAPPED_MAX."""
+    import re
+    text = open(os.path.join(ROOT, "include", "hkv.h")).read()
+    m = re.search(r"#define HKV_HOST_SLAB_MAPPED_MAX \((\d+)ull << (\d+)\)", text)
+    assert m and bench.HOST_SLAB_MAPPED_MAX == int(m.group(1)) << int(m.group(2))
+    assert bench.slab_kinds(bench.HOST_SLAB_MAPPED_MAX) == (2, 3)
+    assert bench.slab_kinds(bench.HOST_SLAB_MAPPED_MAX + 1) == (6, 7)
