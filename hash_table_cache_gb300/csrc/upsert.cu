@@ -176,10 +176,16 @@ constexpr int kStageKeysPerThread = HKV_STAGE_KEYS_PER_THREAD;
 // kWarpDedup: lanes of a warp holding the same key let only the highest
 // (largest batch index) enter the stage, so a key repeated many times in a
 // skewed batch costs fewer atomics on its one address (not under the LFU
-// policies, where every occurrence adds its own increment).  Used for sparse
+// policies, where every occurrence adds its own increment).  Also, the warps
+// take the batch's 32-key chunks from the last to the first, and an
+// occurrence reads its stage position before touching it: it skips the CAS
+// when the key is there already and the max when the recorded index is not
+// below its own (a stale read is only ever lower than the true value, so a
+// skip is always right), which leaves a hot key's later occurrences, most
+// of them seen after its last one, no atomics at all.  Used for sparse
 // batches (at most 4 keys per bucket), where skewed workloads over large
 // tables live; dense batches run the plain kernel, which keeps more blocks
-// resident.
+// resident and whose keys rarely repeat.
 template <bool kWarpDedup>
 __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScratch sc, uint64_t n,
                                                          const uint64_t* keys,
@@ -190,14 +196,18 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
   const uint64_t S = sc.map_size, mask = S - 1, B = t.num_buckets;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   unsigned long long reserved = 0;
+  const uint64_t chunks = (n + 31) / 32;  // kWarpDedup: visited last to first
   // (with kWarpDedup the trip count is warp-uniform: whole warps iterate)
-  for (uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       (kWarpDedup ? i0 - lane_id() : i0) < n; i0 += stride * U) {
+  for (uint64_t j0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       (kWarpDedup ? j0 - lane_id() : j0) < n; j0 += stride * U) {
     uint64_t k[U], pos[U], b[U];
     bool v[U];
+    uint64_t idx[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint64_t i = i0 + u * stride;
+      const uint64_t j = j0 + u * stride;
+      const uint64_t i = kWarpDedup ? (chunks - 1 - (j >> 5)) * 32 + (j & 31) : j;
+      idx[u] = i;
       v[u] = i < n;
       k[u] = v[u] ? keys[i] : kEmptyKey;
       if (v[u] && is_reserved(k[u])) {
@@ -214,9 +224,11 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
     }
     unsigned long long prev[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (v[u]) prev[u] = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + pos[u]),
-                                   kEmptyKey, k[u]);
+    for (int u = 0; u < U; ++u) {
+      if (!v[u]) continue;
+      unsigned long long* q = reinterpret_cast<unsigned long long*>(sc.map_keys + pos[u]);
+      prev[u] = (kWarpDedup && __ldcg(q) == k[u]) ? k[u] : atomicCAS(q, kEmptyKey, k[u]);
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!v[u]) continue;
@@ -227,9 +239,10 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
         p = (p + 1) & mask;
         pv = atomicCAS(reinterpret_cast<unsigned long long*>(sc.map_keys + p), kEmptyKey, k[u]);
       }
-      atomicMax(sc.map_idx + p, static_cast<uint32_t>(i0 + u * stride) + 1);
+      const uint32_t mine = static_cast<uint32_t>(idx[u]) + 1;
+      if (!kWarpDedup || __ldcg(sc.map_idx + p) < mine) atomicMax(sc.map_idx + p, mine);
       // LFU policies: every occurrence adds its increment to the entry's sum
-      if (sc.inc) atomic_add_sat64(sc.inc + p, inc_in ? inc_in[i0 + u * stride] : 1ull);
+      if (sc.inc) atomic_add_sat64(sc.inc + p, inc_in ? inc_in[idx[u]] : 1ull);
       // Sparse batches mark the buckets they touch (plain store) so that the
       // processing kernel skips the others without reading them; dense
       // batches skip the marks, which would only collide.
