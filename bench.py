@@ -564,7 +564,7 @@ def c2_steps(ctx, args, seed_base, world):
             "counts": counts, "hit_rate": hit_rate, "clocks": clk.summary(), "nsteps": nsteps}
 
 
-def api_calls(ctx, st):
+def api_calls(ctx, st, peak):
     """The other calls of the API on the same full table, one 2^20-key batch
     each (median of 3, L2 flushed before each)."""
     torch, hkv = ctx.torch, ctx.hkv
@@ -579,8 +579,13 @@ def api_calls(ctx, st):
     api["find_ptr_bkvs"] = BATCH / statistics.median(
         [ctx.timed(lambda: hkv.hkv_find_ptr(t.handle, BATCH, qk, ptr_out, fout, sout))
          for _ in range(3)]) / 1e9
-    api["assign_bkvs"] = BATCH / statistics.median(
-        [ctx.timed(lambda: t.assign(qk, qv, None)) for _ in range(3)]) / 1e9
+    ta = statistics.median([ctx.timed(lambda: t.assign(qk, qv, None)) for _ in range(3)])
+    api["assign_bkvs"] = BATCH / ta / 1e9
+    # assign's algorithmic bytes: a hit as assign_bytes_per_hit, a miss its
+    # key and digest line
+    hits = int(t.contains(qk).sum().item())
+    api["assign_frac"] = (hits * assign_bytes_per_hit(DIM)
+                          + (BATCH - hits) * (8 + 128)) / ta / (peak * 1e9)
     ek = torch.empty(BATCH, dtype=torch.int64, device=ctx.dev)
     ev_ = torch.empty((BATCH, DIM), dtype=torch.float32, device=ctx.dev)
     es = torch.empty(BATCH, dtype=torch.int64, device=ctx.dev)
@@ -1019,7 +1024,7 @@ def run_gpu(args):
                           "in flight and blocks per SM) + streamed bytes at the copy peak"}
     except Exception as exc:  # the probe is a measurement aid; the line stands without it
         access = {"unavailable": str(exc)}
-    api = api_calls(ctx, st)
+    api = api_calls(ctx, st, peak)
     e2e = end_to_end(ctx, st, args.steps, world) if (rank == 0 or world > 1) else None
     st["table"].close()
     clocks = st["clocks"]
