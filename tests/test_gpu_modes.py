@@ -219,10 +219,12 @@ def test_dual_counts_mixed_batches(hkv, oracle_mod, policy):
     assert t.error_counts()["timeouts"] == 0
 
 
-def test_tiered_equals_hbm_only(hkv, oracle_mod):
+@pytest.mark.parametrize("dim", [16, 6, 132])
+def test_tiered_equals_hbm_only(hkv, oracle_mod, dim):
     """Tiered mode (HKV §3.6): with half of the value rows in mapped host
-    memory every result equals an HBM-only twin bit for bit."""
-    B, dim = 512, 16
+    memory every result equals an HBM-only twin bit for bit (dim 6 and 132
+    take the find kernel's any-width row copy)."""
+    B = 512
     cap = B * 128
     budget = (B // 2) * 128 * 4 * dim
     t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=budget)
@@ -247,6 +249,40 @@ def test_tiered_equals_hbm_only(hkv, oracle_mod):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_tiered_pool_slab_equals_hbm_only(hkv):
+    """A host slab larger than HKV_HOST_SLAB_MAPPED_MAX comes from a host-NUMA
+    memory pool (2^27 slots of 64 floats with a 4 GiB HBM budget: 28 GiB of
+    rows on the host); every result still equals an HBM-only twin bit for
+    bit: finds, assign, export of a host-row slot range."""
+    cap, dim, n = 1 << 27, 64, 1 << 20
+    budget = 4 << 30
+    t = hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED, value_hbm_bytes=budget)
+    h = hkv.HashTable(cap, dim)
+    info = t.info()
+    assert info["hbm_value_rows"] == budget // (4 * dim) and info["host_values_addr"] != 0
+    keys = wl.unique_keys(97, 5 * n)
+    for i in range(5):
+        k = dkeys(keys[i * n:(i + 1) * n])
+        v = wl.key_values_torch(k, dim, salt=10 + i)
+        for x in (t, h):
+            x.insert_or_assign(k, v, None)
+    a = dkeys(keys[::7])
+    av = wl.key_values_torch(a, dim, salt=50)
+    for x in (t, h):
+        x.assign(a, av, None)
+    for lo in range(0, keys.size, n):
+        q = dkeys(np.concatenate([keys[lo:lo + n:2], wl.unique_keys(98 + lo, n // 8)]))
+        ra, rb = t.find(q), h.find(q)
+        torch.cuda.synchronize()
+        for x, y in zip(ra, rb):
+            assert torch.equal(x, y)
+    lo = 3 << 25  # slots far above the HBM rows
+    for x, y in zip(t.export(lo, lo + (1 << 18)), h.export(lo, lo + (1 << 18))):
+        assert torch.equal(x, y)
+    t.close()
+    h.close()
 
 
 def test_roles_across_streams(hkv, oracle_mod):
