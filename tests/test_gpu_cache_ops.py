@@ -27,11 +27,16 @@ def oracle_mod():
     return oracle
 
 
-@pytest.mark.parametrize("num_buckets,dim", [(1, 4), (16, 8), (300, 3)])
-def test_insert_and_evict_and_find_or_insert(hkv, oracle_mod, num_buckets, dim):
+@pytest.mark.parametrize("num_buckets,dim,tiered", [(1, 4, False), (16, 8, False), (300, 3, False),
+                                                    (16, 8, True), (300, 4, True)])
+def test_insert_and_evict_and_find_or_insert(hkv, oracle_mod, num_buckets, dim, tiered):
+    """tiered: the rows of buckets past the first half live in host memory,
+    so evicted rows are copied out of it (still equal to the oracle)."""
     rng = np.random.default_rng(num_buckets)
     cap = num_buckets * 128
-    t = hkv.HashTable(cap, dim)
+    t = (hkv.HashTable(cap, dim, mode=hkv.HKV_MODE_TIERED,
+                       value_hbm_bytes=(num_buckets // 2) * 128 * 4 * dim)
+         if tiered else hkv.HashTable(cap, dim))
     o = oracle_mod.OracleTable(num_buckets, dim)
     universe = wl.unique_keys(500 + num_buckets, 3 * cap)
     for step in range(16):
