@@ -189,15 +189,18 @@ bool batch_ok(hkv_table* t, uint64_t n) { return t && n <= HKV_MAX_BATCH; }
 // memory reads fastest while the process's mapped footprint stays small, and
 // falls steeply past it; pool memory reads more slowly but holds its rate at
 // any size (figures in include/hkv.h).
+cudaError_t alloc_mapped_slab(size_t bytes, void** host, void** slab) {
+  cudaError_t e = cudaHostAlloc(host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(slab, *host, 0);
+  return e;
+}
+
 cudaError_t alloc_host_slab(int device, size_t bytes, cudaMemPool_t* pool, void** host,
                             void** slab) {
   *pool = nullptr;
   *host = nullptr;
-  if (bytes <= HKV_HOST_SLAB_MAPPED_MAX) {
-    cudaError_t e = cudaHostAlloc(host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-    if (e == cudaSuccess) e = cudaHostGetDevicePointer(slab, *host, 0);
-    return e;
-  }
+  *slab = nullptr;
+  if (bytes <= HKV_HOST_SLAB_MAPPED_MAX) return alloc_mapped_slab(bytes, host, slab);
   int numa = -1;
   if (cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, device) != cudaSuccess) {
     cudaGetLastError();
@@ -208,19 +211,27 @@ cudaError_t alloc_host_slab(int device, size_t bytes, cudaMemPool_t* pool, void*
   props.location.type = numa >= 0 ? cudaMemLocationTypeHostNuma : cudaMemLocationTypeHost;
   props.location.id = numa >= 0 ? numa : 0;
   cudaError_t e = cudaMemPoolCreate(pool, &props);
-  if (e != cudaSuccess) {
-    *pool = nullptr;
-    return e;
+  if (e == cudaSuccess) {
+    cudaMemAccessDesc access{};
+    access.location.type = cudaMemLocationTypeDevice;
+    access.location.id = device;
+    access.flags = cudaMemAccessFlagsProtReadWrite;
+    e = cudaMemPoolSetAccess(*pool, &access, 1);
   }
-  cudaMemAccessDesc access{};
-  access.location.type = cudaMemLocationTypeDevice;
-  access.location.id = device;
-  access.flags = cudaMemAccessFlagsProtReadWrite;
-  e = cudaMemPoolSetAccess(*pool, &access, 1);
   if (e == cudaSuccess) e = cudaMallocFromPoolAsync(slab, bytes, *pool, cudaStreamLegacy);
   if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamLegacy);
-  if (e == cudaSuccess) *host = *slab;
-  return e;
+  if (e == cudaSuccess) {
+    *host = *slab;
+    return e;
+  }
+  // no host memory pool here (or it could not hold the slab): mapped memory,
+  // at its lower rate for random rows past HKV_HOST_SLAB_MAPPED_MAX
+  if (*slab) cudaFree(*slab);
+  if (*pool) cudaMemPoolDestroy(*pool);
+  *pool = nullptr;
+  *slab = nullptr;
+  cudaGetLastError();
+  return alloc_mapped_slab(bytes, host, slab);
 }
 
 bool clock_policy(const hkv_table* t) {

@@ -144,7 +144,9 @@ hkv_status hkv_create(uint64_t capacity, uint32_t dim, uint32_t mode, uint64_t v
  * C2C), random 256-byte row reads from the GPU: mapped memory reads at 183-208
  * GB/s while the process's mapped footprint is at most 16 GiB and at 7-12
  * GB/s beyond 24 GiB; pool memory reads at 26-28 GB/s from 8 GiB to 32 GiB.
- * Either way a row's device address is fixed for the table's life. */
+ * Where the system offers no host memory pool, a larger slab is mapped
+ * memory too.  Either way a row's device address is fixed for the table's
+ * life. */
 #define HKV_HOST_SLAB_MAPPED_MAX (16ull << 30)
 
 /* Wait for all work on the table and free it.  NULL is a no-op. */
