@@ -85,18 +85,32 @@ __device__ __forceinline__ bool absent_in_call(const UpsertScratch& sc, uint64_t
 // Map entry of `key` when batch index i is its last occurrence, else kNone,
 // looked up by one thread (the warp-per-32-keys kernels keep a warp's 32
 // lookups in flight together).  Each probe position's key and index are read together.
-__device__ __forceinline__ uint32_t map_last_occurrence(const UpsertScratch& sc, uint64_t key,
-                                                        uint64_t i) {
+// The lookup in two steps, so that a kernel can start it (the home
+// position's key and index in flight), issue other loads, and finish it.
+struct MapProbe {
+  uint32_t s;    // position
+  uint32_t idx;  // its index
+  uint64_t v;    // its key
+};
+__device__ __forceinline__ MapProbe map_probe_start(const UpsertScratch& sc, uint64_t key) {
+  const uint32_t s = map_home(key, sc.map_size - 1);
+  return MapProbe{s, sc.map_idx[s], sc.map_keys[s]};
+}
+__device__ __forceinline__ uint32_t map_last_occurrence_from(const UpsertScratch& sc, uint64_t key,
+                                                             uint64_t i, MapProbe f) {
   const uint32_t mask = sc.map_size - 1;
-  uint32_t s = map_home(key, mask);
   for (uint32_t p = 0; p <= mask; ++p) {
-    const uint64_t v = sc.map_keys[s];
-    const uint32_t idx = sc.map_idx[s];
-    if (v == key) return idx == static_cast<uint32_t>(i) + 1 ? s : kNone;
-    if (v == kEmptyKey) return kNone;
-    s = (s + 1) & mask;
+    if (f.v == key) return f.idx == static_cast<uint32_t>(i) + 1 ? f.s : kNone;
+    if (f.v == kEmptyKey) return kNone;
+    f.s = (f.s + 1) & mask;
+    f.v = sc.map_keys[f.s];
+    f.idx = sc.map_idx[f.s];
   }
   return kNone;
+}
+__device__ __forceinline__ uint32_t map_last_occurrence(const UpsertScratch& sc, uint64_t key,
+                                                        uint64_t i) {
+  return map_last_occurrence_from(sc, key, i, map_probe_start(sc, key));
 }
 
 // Summed increment of a deduplicated entry (LFU policies; 0 otherwise).
@@ -1720,15 +1734,19 @@ __global__ void __launch_bounds__(kThreads, HKV_ASSIGN_MIN_BLOCKS) assign_kernel
        base < n; base += warps * 32) {
     const uint64_t i = base + lane;
     const uint64_t k = i < n ? keys[i] : kEmptyKey;
-    const uint32_t ms = i < n && !is_reserved(k) ? map_last_occurrence(sc, k, i) : kNone;
-    const bool live = ms != kNone;  // the key's last occurrence in the batch
+    const bool valid = i < n && !is_reserved(k);
+    // the dedup lookup's first position is read while the digest lines load
+    MapProbe mp{0, 0, 0};
+    if (valid) mp = map_probe_start(sc, k);
     const uint64_t h = hash64(k);
     const uint32_t b1 = static_cast<uint32_t>(bucket_of_hash(t, h));
     const uint32_t b2 = kDual ? static_cast<uint32_t>(bucket2_of(t, k, b1)) : b1;
-    const unsigned probe = __ballot_sync(kFull, live);
+    const unsigned probe = __ballot_sync(kFull, valid);
     if (!probe) continue;
     uint4 c1, c2;
     warp_candidates<kDual>(t, probe, b1, b2, digest_of_hash(h) * 0x01010101u, lane, msk, c1, c2);
+    const uint32_t ms = valid ? map_last_occurrence_from(sc, k, i, mp) : kNone;
+    const bool live = ms != kNone;  // the key's last occurrence in the batch
     uint32_t bk = b1;
     const int slot = live ? confirm_slot(t, k, b1, b2, c1, c2, bk) : -1;
     if (slot >= 0) {
