@@ -44,6 +44,7 @@ HKV_ERR_RESERVED_KEY = -4
 HKV_ERR_TIMEOUT = -5
 SLOTS_PER_BUCKET = 128
 RESERVED_KEY_LO = 0xFFFFFFFFFFFFFFF0
+HKV_MAX_BATCH = 0x7FFFFFFF  # largest n a batched call accepts
 
 # Every symbol include/hkv.h declares (checked by the CPU test suite).
 EXPORTS = (

@@ -193,3 +193,42 @@ def test_edge_cases(hkv, oracle_mod):
     find_compare(t, o, r)
     assert t.error_counts()["reserved"] >= 6
     assert_same_state(t, o)
+
+
+@pytest.mark.parametrize("mode", ["single", "dual", "tiered"])
+def test_empty_and_oversized_batches(hkv, mode):
+    """n = 0 is a valid batch for every batched call in every mode and changes
+    nothing; n above HKV_MAX_BATCH is refused with HKV_ERR_INVALID before any
+    pointer is used; dual mode refuses insert_and_evict and find_or_insert
+    whatever n is (HKV §7: its calls are find and insert_or_assign)."""
+    B, dim = 64, 4
+    cap = B * 128
+    m = {"single": 0, "dual": hkv.HKV_MODE_DUAL, "tiered": hkv.HKV_MODE_TIERED}[mode]
+    kw = {"value_hbm_bytes": (B // 2) * 128 * 4 * dim} if mode == "tiered" else {}
+    t = hkv.HashTable(cap, dim, mode=m, **kw)
+    k = dkeys(wl.unique_keys(700, 3000))
+    t.insert_or_assign(k, wl.key_values_torch(k, dim, salt=1), None)
+    torch.cuda.synchronize()
+    before = table_state(t)
+    s0, c0 = t.size(), t.op_counts()
+    h, OK, INV = t.handle, hkv.HKV_OK, hkv.HKV_ERR_INVALID
+    ev_keys = torch.zeros(1, dtype=torch.int64, device=DEV)
+    ev_count = torch.zeros(1, dtype=torch.int64, device=DEV)
+    dual = mode == "dual"
+    for n, want in ((0, OK), (hkv.HKV_MAX_BATCH + 1, INV)):
+        assert hkv.hkv_find(h, n, None, None, None) == want
+        assert hkv.hkv_contains(h, n, None, None) == want
+        assert hkv.hkv_find_ptr(h, n, None, None, None) == want
+        assert hkv.hkv_insert_or_assign(h, n, None, None) == want
+        assert hkv.hkv_insert_or_assign_noalloc(h, n, None, None) == want
+        assert hkv.hkv_assign(h, n, None, None) == want
+        assert hkv.hkv_erase(h, n, None) == want
+        assert hkv.hkv_insert_and_evict(h, n, None, None, None, ev_keys, None, None,
+                                        ev_count) == (INV if dual else want)
+        assert hkv.hkv_find_or_insert(h, n, None, None, None, None) == (INV if dual else want)
+    torch.cuda.synchronize()
+    assert int(ev_count.item()) == 0
+    assert t.size() == s0 and t.op_counts() == c0
+    for x, y in zip(before, table_state(t)):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    t.close()
