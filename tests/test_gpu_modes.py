@@ -174,6 +174,44 @@ def test_dual_bucket_invariants(hkv, oracle_mod):
     assert tot_free <= 0.01 * tot_absent and tot_weak <= 0.01 * tot_absent
 
 
+@pytest.mark.parametrize("bs", [1, 37, 300])
+def test_dual_two_buckets(hkv, oracle_mod, bs):
+    """The smallest dual table, B = 2: every key's two candidate buckets are
+    the whole table (b2 is always the other bucket).  Batches of one key up
+    to more than the table's 256 slots, unique random scores: after every
+    batch the counts add up and, every fourth batch and at the end, the
+    invariants hold; once both buckets are full no absent key has a free
+    candidate bucket."""
+    B, dim = 2, 4
+    t = hkv.HashTable(B * 128, dim, mode=hkv.HKV_MODE_DUAL)
+    o = oracle_mod.OracleTable(B, dim, dual=True)
+    keys = wl.unique_keys(85, 1200)
+    scores = wl.stream(86, keys.size) >> np.uint64(2)
+    last_score, last_salt = {}, {}
+    free_departures = 0
+    for i, lo in enumerate(range(0, keys.size, bs)):
+        k, sc = keys[lo:lo + bs], scores[lo:lo + bs]
+        v = wl.key_values(k, dim, salt=i)
+        t.reset_op_counts()
+        before = t.size()
+        t.insert_or_assign(dkeys(k), dvals(v), dkeys(sc))
+        for kk, ss in zip(k.tolist(), sc.tolist()):
+            last_score[kk], last_salt[kk] = ss, i
+        c = t.op_counts()
+        assert c["admitted"] + c["rejected"] == k.size and c["updated"] == 0
+        assert t.size() == before + c["admitted"] - c["evicted"] <= B * 128
+        assert c["admitted"] == int(t.contains(dkeys(k)).sum().item())
+        if before == B * 128:
+            _, nfree, _ = _first_presentation_check(t, o, k, sc)
+            free_departures += nfree
+        if i % 4 == 3:
+            _check_dual_invariants(t, o, last_score, last_salt, dim)
+    assert t.size() == B * 128
+    _check_dual_invariants(t, o, last_score, last_salt, dim)
+    assert free_departures == 0
+    t.close()
+
+
 @pytest.mark.parametrize("policy", ["custom", "lru"])
 def test_dual_counts_mixed_batches(hkv, oracle_mod, policy):
     """Dual mode on a full table with batches that mix resident keys, fresh
