@@ -50,7 +50,8 @@ def test_c1_insert_then_find(hkv, oracle_mod):
     assert 0 < hits <= n // 2
 
 
-@pytest.mark.parametrize("num_buckets,dim", [(1, 1), (1, 8), (3, 5), (64, 4), (100, 8), (37, 33)])
+@pytest.mark.parametrize("num_buckets,dim", [(1, 1), (1, 8), (3, 5), (64, 4), (100, 8), (37, 33),
+                                             (5, 256), (3, 1001)])
 @pytest.mark.parametrize("seed", [0, 1])
 def test_random_ops_bit_exact(hkv, oracle_mod, num_buckets, dim, seed):
     """Random mixes of insert_or_assign (per-key scores with many ties, or the
@@ -93,7 +94,7 @@ def test_random_ops_bit_exact(hkv, oracle_mod, num_buckets, dim, seed):
 
 
 @pytest.mark.parametrize("policy", ["custom", "lfu"])
-@pytest.mark.parametrize("num_buckets,dim", [(64, 8), (300, 4), (1024, 16)])
+@pytest.mark.parametrize("num_buckets,dim", [(64, 8), (300, 4), (1024, 16), (64, 260)])
 def test_sparse_batches_bit_exact(hkv, oracle_mod, policy, num_buckets, dim):
     """Batches of at most four keys per bucket (the sparse path: one tile per
     touched bucket, the general kernel for the buckets it defers), on tables
