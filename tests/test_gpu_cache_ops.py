@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads as wl
-from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, read_device, u64
+from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, read_device, table_state, u64
 
 pytestmark = pytest.mark.gpu
 
@@ -117,4 +117,35 @@ def test_contains_and_find_ptr(hkv, oracle_mod, mode):
     for i in np.flatnonzero(hit)[:400]:
         row = read_device(p[i], 4 * dim).view(np.float32)
         assert np.array_equal(row, ov[i])
+    t.close()
+
+
+@pytest.mark.parametrize("tiered", [False, True])
+def test_export_score_threshold(hkv, oracle_mod, tiered):
+    """export with a score threshold (HKV §4.1 export_batch_if, predicate
+    score >= threshold; DynamicEmb incremental_dump): for thresholds from 0
+    past the largest score, over the whole table and over bucket ranges, the
+    entries equal the oracle's bit for bit (keys, values, scores)."""
+    B, dim = 96, 6
+    cap = B * 128
+    kw = {"mode": hkv.HKV_MODE_TIERED, "value_hbm_bytes": (B // 3) * 128 * 4 * dim} if tiered else {}
+    t = hkv.HashTable(cap, dim, **kw)
+    o = oracle_mod.OracleTable(B, dim)
+    rng = np.random.default_rng(9)
+    keys = wl.unique_keys(710, int(1.3 * cap))
+    for lo in range(0, keys.size, 3000):
+        k = keys[lo:lo + 3000]
+        v = wl.key_values(k, dim, salt=lo)
+        sc = rng.integers(0, 1000, k.size).astype(np.uint64)
+        t.insert_or_assign(dkeys(k), dvals(v), dkeys(sc))
+        o.insert_or_assign(k, v, sc)
+    torch.cuda.synchronize()
+    for thr in (0, 1, 500, 990, 999, 1000, 1 << 62):
+        for b0, b1 in ((0, B), (0, 1), (17, 18), (40, 71), (B - 1, B)):
+            gk, gv, gs = table_state(t, b0 * 128, b1 * 128, thr)
+            ok, ov, os_ = o.export(b0, b1, thr)
+            assert np.array_equal(gk, ok), (thr, b0, b1)
+            assert np.array_equal(gs, os_)
+            assert np.array_equal(gv.view(np.uint32), ov.view(np.uint32))
+            assert np.all(gs >= thr)
     t.close()
