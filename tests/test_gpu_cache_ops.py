@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads as wl
-from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, read_device, table_state, u64
+from tests.gpu_util import assert_same_state, dkeys, dvals, read_device, table_state, u64
 
 pytestmark = pytest.mark.gpu
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import workloads as wl
-from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, find_compare, table_state, u64
+from tests.gpu_util import DEV, assert_same_state, dkeys, dvals, table_state, u64
 
 pytestmark = pytest.mark.gpu
 

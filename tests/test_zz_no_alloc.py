@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import workloads as wl
-from tests.gpu_util import dkeys, dvals, table_state, u64
+from tests.gpu_util import dkeys, dvals, table_state
 
 pytestmark = pytest.mark.gpu
 
