@@ -1,5 +1,6 @@
 """The seeded input generators (CPU only)."""
 import numpy as np
+import pytest
 import torch
 
 import workloads as wl
@@ -39,3 +40,28 @@ def test_hit_mix_fraction():
     assert drawn.sum() == 16000
     assert np.isin(keys[drawn], res).all()
     assert not np.isin(keys[~drawn], res).any()
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.99, 1.25])
+def test_zipf_torch_sampler_distribution(alpha):
+    """The device sampler draws ranks with the Zipf(alpha) probabilities
+    r^-alpha / sum(r^-alpha) over 1..U (U = 1000, exact): each of the top
+    ranks' frequency within 5 standard deviations, Pearson's chi-square over
+    all U ranks within 6 standard deviations of its mean (U - 1 degrees of
+    freedom), and rank r maps to the host sampler's key for r."""
+    import torch
+    U, n = 1000, 1 << 20
+    keys = wl.zipf_keys_torch(7, n, alpha, U, "cpu").numpy().view(np.uint64)
+    ranks = np.arange(1, U + 1, dtype=np.uint64)
+    key_of = wl.mix(ranks + np.uint64(0x2545F4914F6CDD1D))
+    pos = {int(k): i for i, k in enumerate(key_of)}
+    idx = np.array([pos[int(k)] for k in keys])  # every key is some rank's key
+    counts = np.bincount(idx, minlength=U)
+    p = ranks.astype(np.float64) ** -alpha
+    p /= p.sum()
+    emp = counts / n
+    for r in range(20):
+        sd = np.sqrt(p[r] * (1 - p[r]) / n)
+        assert abs(emp[r] - p[r]) < 5 * sd, (r + 1, emp[r], p[r])
+    chi2 = float((((counts - n * p) ** 2) / (n * p)).sum())
+    assert chi2 < (U - 1) + 6 * np.sqrt(2 * (U - 1)), chi2

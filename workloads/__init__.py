@@ -149,6 +149,32 @@ def zipf_keys(seed: int, n: int, alpha: float, universe: int, salt: int = 0x2545
         return _check_keys(mix(r + _U(salt)))
 
 
+def zipf_keys_torch(seed: int, n: int, alpha: float, universe: int, device,
+                    salt: int = 0x2545F4914F6CDD1D):
+    """Keys of ``zipf_keys``' distribution drawn on a torch device: the same
+    rejection-inversion sampler over ranks 1..universe (``Zipf``'s
+    constants), its uniforms from a seeded torch generator on ``device`` (so
+    not the same draws as ``zipf_keys``), rank r mapped to the key
+    mix(r + salt).  Returns an int64 tensor holding the uint64 bits."""
+    import torch
+    z = Zipf(alpha, universe)
+    q = z.q
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = torch.empty(n, dtype=torch.int64, device=device)
+    todo = torch.arange(n, device=device)
+    while todo.numel():
+        u = torch.rand(todo.numel(), dtype=torch.float64, generator=g, device=device)
+        y = z.hn + u * (z.hx1 - z.hn)
+        x = torch.pow(1.0 + y * (1.0 - q), 1.0 / (1.0 - q))
+        k = torch.clamp(torch.floor(x + 0.5), 1, z.n)
+        hk = (torch.pow(k + 0.5, 1.0 - q) - 1.0) / (1.0 - q) - torch.pow(k, -q)
+        ok = (k - x <= z.s) | (y >= hk)
+        out[todo[ok]] = k[ok].to(torch.int64)
+        todo = todo[~ok]
+    return _mix_torch(out + _i64(salt))
+
+
 # --------------------------------------------------------------------------
 # Values.
 # --------------------------------------------------------------------------
