@@ -60,6 +60,18 @@ constexpr int kBucketThreads = HKV_BUCKET_THREADS;  // bucket kernel block size
 #endif
 constexpr uint32_t kHitMark = 0x80000000u;
 
+// Saturating add of v to a per-call sum of LFU increments: one native
+// atomicAdd, and if the old value shows that this add wrapped past 2^64 - 1,
+// an atomicMax that pins the sum at 2^64 - 1 (every later add wraps again and
+// pins it again; a sum that never reaches 2^64 never wraps and is exact).
+// Unlike a compare-and-swap loop it costs one operation however many
+// occurrences of one hot key add at once.
+__device__ __forceinline__ void sum_add_sat64(uint64_t* p, uint64_t v) {
+  unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
+  const unsigned long long old = atomicAdd(q, static_cast<unsigned long long>(v));
+  if (old + v < old) atomicMax(q, ~0ull);
+}
+
 __device__ __forceinline__ uint32_t map_home(uint64_t key, uint32_t mask) {
   return static_cast<uint32_t>(hash64(key) >> 32) & mask;
 }
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) dedup_insert_kernel(UpsertScratch sc
     }
     if (sc.inc) {  // warp-uniform
       slot = __shfl_sync(0xFFFFFFFFu, slot, lead);
-      if (valid && slot != kNone) atomic_add_sat64(sc.inc + slot, inc_in ? inc_in[i] : 1ull);
+      if (valid && slot != kNone) sum_add_sat64(sc.inc + slot, inc_in ? inc_in[i] : 1ull);
     }
   }
   warp_add(&stats->reserved, reserved);
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) stage_kernel(TableView t, UpsertScra
       const uint32_t mine = static_cast<uint32_t>(idx[u]) + 1;
       if (!kWarpDedup || __ldcg(sc.map_idx + p) < mine) atomicMax(sc.map_idx + p, mine);
       // LFU policies: every occurrence adds its increment to the entry's sum
-      if (sc.inc) atomic_add_sat64(sc.inc + p, inc_in ? inc_in[idx[u]] : 1ull);
+      if (sc.inc) sum_add_sat64(sc.inc + p, inc_in ? inc_in[idx[u]] : 1ull);
       // Sparse batches mark the buckets they touch (plain store) so that the
       // processing kernel skips the others without reading them; dense
       // batches skip the marks, which would only collide.

@@ -190,3 +190,60 @@ def test_dual_mode_policy_invariants(hkv, oracle_mod, policy):
         assert np.array_equal(scores >> np.uint64(32), le)
         assert np.all((scores & np.uint64(0xFFFFFFFF)) >= 1)
     t.close()
+
+
+@pytest.mark.parametrize("policy", POLICIES)
+def test_zipf_ingestion_hits_equal_oracle(hkv, oracle_mod, policy):
+    """The policy sweep's procedure (HKV §5.4 Exp #3c) at a small scale: a
+    2^14-slot table takes batches of Zipf(0.99) keys over 2^19, each looked
+    up (contains) and then inserted with the policy's score (customized: the
+    step; epoch policies: a new epoch every step).  Every batch's hit count
+    and the table after it equal the oracle's, so the sweep's hit rates come
+    from the table evolution Algorithm 2 defines."""
+    lib_code, ora_code = _codes(hkv, oracle_mod, policy)
+    B, dim, n = 128, 4, 1 << 12
+    t = hkv.HashTable(B * 128, dim, mode=lib_code)
+    o = oracle_mod.OracleTable(B, dim, policy=ora_code)
+    zeros = np.zeros((n, dim), np.float32)
+    hits = []
+    for step in range(1, 13):
+        k = wl.zipf_keys(300 + step, n, 0.99, 1 << 19)
+        if policy.startswith("epoch"):
+            t.set_epoch(step)
+            o.set_epoch(step)
+        sc = np.full(n, step, np.uint64) if policy == "customized" else None
+        g = int(t.contains(dkeys(k)).sum().item())
+        _, of, _ = o.find(k)
+        assert g == int(of.sum()), (step, g, int(of.sum()))
+        hits.append(g)
+        t.insert_or_assign(dkeys(k), dvals(zeros), None if sc is None else dkeys(sc))
+        o.insert_or_assign(k, zeros, sc)
+        assert_same_state(t, o)
+    assert hits[-1] > hits[1] > 0  # the hot keys settle in
+    t.close()
+
+
+def test_lfu_increment_sums_saturate(hkv, oracle_mod):
+    """LFU increments summed per key within a call, and added to a resident
+    key's score, saturate at 2^64 - 1 (the policy's add): one key repeated
+    with increments of 2^63 and 2^63 - 1 in one batch, then more in later
+    calls, gives the oracle's scores bit for bit."""
+    lib_code, ora_code = _codes(hkv, oracle_mod, "lfu")
+    B, dim = 4, 2
+    t = hkv.HashTable(B * 128, dim, mode=lib_code)
+    o = oracle_mod.OracleTable(B, dim, policy=ora_code)
+    keys = wl.unique_keys(720, 64)
+    rng = np.random.default_rng(721)
+    for step in range(6):
+        k = np.concatenate([np.repeat(keys[:3], 40), keys[3 + step * 8:11 + step * 8]])
+        big = np.array([1 << 63, (1 << 63) - 1, 1, 0], np.uint64)
+        inc = big[rng.integers(0, big.size, k.size)] if step % 2 == 0 else \
+            rng.integers(0, 1 << 62, k.size).astype(np.uint64)
+        v = wl.key_values(k, dim, salt=step)
+        t.insert_or_assign(dkeys(k), dvals(v), dkeys(inc))
+        o.insert_or_assign(k, v, inc)
+        assert_same_state(t, o)
+    _, _, gs = t.find(dkeys(keys[:3]))
+    torch.cuda.synchronize()
+    assert np.all(u64(gs) == np.uint64(2 ** 64 - 1))
+    t.close()
