@@ -258,8 +258,8 @@ def rows_of_ptrs(ptrs, found, info):
 NCU_TRAFFIC = {
     "find_kernel": {"bytes": 269957291, "sources": ("find.cu", "common.cuh", "launch.h"),
                     "sha256": "4dee867c0f4192e6"},
-    "upsert_single_kernel": {"bytes": 330468949, "sources": ("upsert.cu", "common.cuh", "launch.h"),
-                             "sha256": "9b05596280c9a1fb"},
+    "upsert_single_kernel": {"bytes": 330548651, "sources": ("upsert.cu", "common.cuh", "launch.h"),
+                             "sha256": "df235f4f136a45f4"},
 }
 
 
@@ -1345,6 +1345,73 @@ def run_probe_sweep():
                       "host_rows_by_buffer_size_GB_per_s": slab}))
 
 
+POLICY_SWEEP_ALPHAS = (0.5, 0.75, 0.99, 1.25)
+
+
+def run_policy_sweep(args):
+    """Cache hit rate by score policy and Zipf exponent (HKV §5.4 Exp #3c,
+    Table 8): a 2^27-slot single-bucket table of 32-float rows (the pages'
+    Config B), keys Zipf(alpha) over 2^32, batches of 2^20.  The table is
+    warmed up with 2 x capacity keys of the stream (it fills to load factor
+    1.0 and turns over once), then each of `args.steps` batches is looked up
+    (contains: a hit is a key found) and inserted (insert_or_assign with the
+    policy's score: customized gets the step as its score, the epoch
+    policies a new epoch every step).  Also each policy's rate over the
+    measured steps (lookups + inserts per second).  One JSON object."""
+    import torch
+    ctx = Ctx(0)
+    hkv = ctx.hkv
+    hkv.load()
+    cap, dim, n, universe, warm_batch = 1 << 27, 32, 1 << 20, 1 << 32, 1 << 23
+    policies = (("customized", hkv.HKV_POLICY_CUSTOMIZED), ("lru", hkv.HKV_POLICY_LRU),
+                ("lfu", hkv.HKV_POLICY_LFU), ("epoch_lru", hkv.HKV_POLICY_EPOCH_LRU),
+                ("epoch_lfu", hkv.HKV_POLICY_EPOCH_LFU))
+    zeros = torch.zeros((warm_batch, dim), device=ctx.dev)  # values do not affect hits
+    hit_rate = {name: {} for name, _ in policies}
+    rate = {name: [] for name, _ in policies}
+    for ai, alpha in enumerate(POLICY_SWEEP_ALPHAS):
+        warm = [wl.zipf_keys_torch(1000 + 100 * ai + i, warm_batch, alpha, universe, ctx.dev)
+                for i in range(2 * cap // warm_batch)]
+        meas = [wl.zipf_keys_torch(2000 + 100 * ai + i, n, alpha, universe, ctx.dev)
+                for i in range(args.steps)]
+        for name, code in policies:
+            t = hkv.HashTable(cap, dim, mode=code, device=ctx.local)
+            step = 0
+
+            def put(k):
+                nonlocal step
+                step += 1
+                if name.startswith("epoch"):
+                    t.set_epoch(step)
+                sc = (torch.full((k.numel(),), step, dtype=torch.int64, device=ctx.dev)
+                      if name == "customized" else None)
+                t.insert_or_assign(k, zeros[:k.numel()], sc)
+
+            for k in warm:
+                put(k)
+            hits = torch.zeros((), dtype=torch.int64, device=ctx.dev)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for k in meas:
+                hits += t.contains(k).sum()
+                put(k)
+            b.record()
+            b.synchronize()
+            hit_rate[name][str(alpha)] = round(float(hits.item()) / (args.steps * n), 4)
+            rate[name].append(2 * n * args.steps / (a.elapsed_time(b) * 1e-3) / 1e9)
+            t.close()
+        del warm, meas
+    print(json.dumps({
+        "workload": "single-bucket, capacity 2^27, dim 32 (Config B); Zipf(alpha) over 2^32 in "
+                    "batches of 2^20; warm-up 2 x capacity stream keys, then "
+                    f"{args.steps} batches each looked up (contains) and inserted",
+        "hit_rate": hit_rate,
+        "lookups_and_inserts_bkvs": {k: round(statistics.median(v), 3) for k, v in rate.items()},
+        "data": "synthetic"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1366,6 +1433,9 @@ def main():
     ap.add_argument("--probe-sweep", action="store_true",
                     help="print the random-read rates of this GPU over granule, reads in flight "
                          "and blocks per SM, and the host link by SM access, as one JSON object")
+    ap.add_argument("--policy-sweep", action="store_true",
+                    help="cache hit rate by score policy and Zipf exponent on a 2^27-slot table "
+                         "(the pages' Table 8), as one JSON object; --steps measured batches")
     ap.add_argument("--ablation", choices=["digest", "pipeline"],
                     help="compare the default build with a variant build instead: find without "
                          "the digest line, or the pipelined bucket kernel")
@@ -1374,6 +1444,8 @@ def main():
     args = ap.parse_args()
     if args.probe_sweep:
         run_probe_sweep()
+    elif args.policy_sweep:
+        run_policy_sweep(args)
     elif args.ablation_child:
         run_ablation_child(args.ablation_child, args.ablation_what)
     elif args.ablation:
